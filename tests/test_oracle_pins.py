@@ -1,0 +1,380 @@
+"""Pins of the oracle to facts outside itself: library routines, closed forms,
+invariants, exact arithmetic and brute force on tiny inputs.  CPU only."""
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import qsa_oracle as O
+
+RNG = np.random.default_rng(1234)
+
+
+# --------------------------------------------------------------------------
+# Number formats
+# --------------------------------------------------------------------------
+
+def test_bf16_rounding_matches_torch_including_ties():
+    x = RNG.standard_normal(200000).astype(np.float32) * np.float32(3.0) ** RNG.integers(-30, 30, 200000)
+    x = x.astype(np.float32)
+    # exact midpoints between neighbouring bf16 values (ties to even)
+    b = torch.from_numpy(RNG.standard_normal(5000).astype(np.float32)).to(torch.bfloat16)
+    bits = b.view(torch.int16).to(torch.int32)
+    mids = ((bits << 16) | 0x8000).to(torch.int32).view(torch.float32).numpy()
+    x = np.concatenate([x, mids, np.float32([0.0, -0.0, 1e-40, -3e-39, 3.3e38])])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_bf16(x.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+    enc = O.bf16_encode(x.astype(np.float64))
+    np.testing.assert_array_equal(O.bf16_decode(enc), want)
+
+
+def test_e4m3_code_table_matches_torch_all_256_codes():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_decode_table()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(got[ok], want[ok])
+    # 254 finite codepoints (+-0 included), as the e4m3 decode patch counts them
+    assert ok.sum() == 254
+
+
+def test_e4m3_rounding_matches_torch_within_range():
+    table = O.e4m3_decode_table()
+    finite = np.unique(table[~np.isnan(table)])
+    mids = (finite[1:] + finite[:-1]) / 2  # exact ties
+    x = np.concatenate([finite, mids, RNG.uniform(-448, 448, 100000),
+                        RNG.standard_normal(50000) * 1e-2, RNG.standard_normal(50000)])
+    x = x.astype(np.float32)  # every tested value is exact in fp32
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.round_e4m3(x.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+    codes = O.e4m3_encode(x.astype(np.float64))
+    want_codes = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # -0 and +0 differ only in sign bit; compare values for zeros
+    nz = want != 0
+    np.testing.assert_array_equal(codes[nz], want_codes[nz])
+
+
+def test_e4m3_saturates_instead_of_nan():
+    got = O.round_e4m3(np.array([448.0, 449.0, 463.9, 464.0, 479.0, 1e6, -1e6, -470.0]))
+    np.testing.assert_array_equal(got, [448, 448, 448, 448, 448, 448, -448, -448])
+
+
+# --------------------------------------------------------------------------
+# RMSNorm and RoPE
+# --------------------------------------------------------------------------
+
+def test_gemma_rmsnorm_matches_torch_rms_norm():
+    x = RNG.standard_normal((7, 128))
+    w = RNG.standard_normal(128) * 0.1
+    want = F.rms_norm(torch.from_numpy(x), (128,), torch.from_numpy(1.0 + w), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.gemma_rmsnorm(x, w, 1e-6), want, rtol=1e-12, atol=1e-12)
+
+
+def test_gemma_rmsnorm_unit_rms_and_scale_invariance():
+    x = RNG.standard_normal((5, 128)) * 3.0
+    y = O.gemma_rmsnorm(x, np.zeros(128), 0.0)
+    np.testing.assert_allclose(np.mean(y * y, axis=-1), 1.0, rtol=1e-12)
+    np.testing.assert_allclose(O.gemma_rmsnorm(17.0 * x, np.zeros(128), 0.0), y, rtol=1e-12)
+
+
+def _table(max_pos=4096, rot=64):
+    half = rot // 2
+    inv = 10000.0 ** (-np.arange(half) * 2.0 / rot)
+    ang = np.arange(max_pos)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1)
+
+
+def test_rope_is_identity_at_zero_and_keeps_tail_and_norm():
+    cs = _table()
+    x = RNG.standard_normal(128)
+    np.testing.assert_allclose(O.rope_neox(x, (0, 0, 0), cs, 64, (0, 0, 0)), x, atol=0)
+    y = O.rope_neox(x, (1234, 1234, 1234), cs, 64, (0, 0, 0))
+    np.testing.assert_array_equal(y[64:], x[64:])
+    np.testing.assert_allclose(np.linalg.norm(y), np.linalg.norm(x), rtol=1e-12)
+
+
+def test_rope_matches_complex_rotation_and_relative_position():
+    cs = _table()
+    x = RNG.standard_normal(128)
+    k = RNG.standard_normal(128)
+    m, n = 1000, 377
+    # NeoX pairs (i, i + 32) as complex numbers rotated by angle pos * inv_freq_i
+    z = (x[:32] + 1j * x[32:64]) * np.exp(1j * m * 10000.0 ** (-np.arange(32) / 32.0))
+    y = O.rope_neox(x, (m, m, m), cs, 64, (0, 0, 0))
+    np.testing.assert_allclose(y[:32], z.real, atol=1e-9)
+    np.testing.assert_allclose(y[32:64], z.imag, atol=1e-9)
+    d1 = O.rope_neox(x, (m,) * 3, cs, 64, (0, 0, 0)) @ O.rope_neox(k, (n,) * 3, cs, 64, (0, 0, 0))
+    d2 = O.rope_neox(x, (m + 50,) * 3, cs, 64, (0, 0, 0)) @ O.rope_neox(k, (n + 50,) * 3, cs, 64, (0, 0, 0))
+    assert abs(d1 - d2) < 1e-9
+
+
+def test_mrope_with_equal_components_equals_1d_rope():
+    cs = _table()
+    x = RNG.standard_normal((3, 128))
+    for p in (0, 5, 999, 4095):
+        np.testing.assert_array_equal(O.rope_neox(x, (p, p, p), cs, 64, (8, 12, 12)),
+                                      O.rope_neox(x, (p, p, p), cs, 64, (0, 0, 0)))
+
+
+def test_mrope_section_table_golden():
+    """Hand-derived component of each of the 32 frequencies for [8, 12, 12]
+    (tests/golden/mrope_components_8_12_12.txt)."""
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "mrope_components_8_12_12.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    want = {int(i): "THW".index(c) for i, c in rows}
+    assert len(want) == 32
+    for i in range(32):
+        assert O.mrope_component(i, (8, 12, 12)) == want[i]
+
+
+def test_mrope_changes_only_its_section():
+    cs = _table()
+    x = RNG.standard_normal(128)
+    a = O.rope_neox(x, (100, 200, 300), cs, 64, (8, 12, 12))
+    b = O.rope_neox(x, (100, 250, 300), cs, 64, (8, 12, 12))
+    changed = {i for i in range(32) if a[i] != b[i] or a[32 + i] != b[32 + i]}
+    assert changed == {i for i in range(32) if O.mrope_component(i, (8, 12, 12)) == 1}
+
+
+# --------------------------------------------------------------------------
+# Compress (stage 1)
+# --------------------------------------------------------------------------
+
+def _cfg(**kw):
+    base = dict(n_heads=4, head_dim=128, rotary_dim=64, compress_ratio=4, token_topk=16,
+                eps=1e-6, index_dtype=O.DTYPE_BF16, state_size=8, cpage=4)
+    base.update(kw)
+    return O.QsaConfig(**base)
+
+
+def test_compress_equal_members_pool_to_the_member():
+    cfg = _cfg()
+    cs = _table()
+    key = RNG.standard_normal(128)
+    w = RNG.standard_normal(128) * 0.1
+    got = O.compress_key(cfg, np.stack([key] * 4), (40, 40, 40), cs, w)
+    want = O.round_bf16(O.rope_neox(O.gemma_rmsnorm(key, w, 1e-6), (40,) * 3, cs, 64, (0, 0, 0)))
+    np.testing.assert_array_equal(got, want)
+
+
+def _history_case(r=4, S=8, split_at=None):
+    """A request with token history h[0..p]; the step holds tokens
+    split_at..p, older tokens sit in the ring."""
+    cfg = _cfg(compress_ratio=r, state_size=S)
+    cs = _table()
+    p = 4 * 10 + r - 1  # completes group 10
+    hist = RNG.standard_normal((p + 1, 128))
+    wq = RNG.standard_normal(128) * 0.1
+    wk = RNG.standard_normal(128) * 0.1
+    start = split_at
+    rows = p - start + 1
+    ring = np.zeros((2, S, 128))
+    for t in range(max(0, start - S), start):
+        ring[1, t % S] = hist[t]
+    ccache = np.zeros((8, cfg.cpage, 128))
+    slots = np.full(rows, -1)
+    g = (p + 1) // r - 1
+    slots[-1] = 3 * cfg.cpage + 1
+    args = dict(projected_q=None, raw_keys=hist[start:p + 1],
+                positions=np.stack([np.arange(start, p + 1)] * 3, axis=1), cos_sin=cs,
+                q_norm_w=wq, k_norm_w=wk, ring=ring, ring_pos=None,
+                ring_block_table=np.array([[1]]), token_to_req=np.zeros(rows, dtype=int),
+                query_start_loc=np.array([0, rows]), logical_positions=np.arange(start, p + 1),
+                ccache=ccache, compressed_slots=slots)
+    return cfg, cs, hist, p, g, wk, args
+
+
+@pytest.mark.parametrize("split_at_back", [0, 1, 2, 3, 5])
+def test_compress_member_source_ring_or_step_is_transparent(split_at_back):
+    """The compressed key of group g depends only on the token history, not
+    on how many of its members arrived in this step (brute force)."""
+    cfg, cs, hist, p, g, wk, args = _history_case(split_at=None or (43 - split_at_back))
+    O.compress_stage(cfg, **args)
+    want = O.round_bf16(O.rope_neox(O.gemma_rmsnorm(hist[g * 4:g * 4 + 4].mean(0), wk, 1e-6),
+                                    (g * 4,) * 3, cs, 64, (0, 0, 0)))
+    np.testing.assert_array_equal(args["ccache"][3, 1], want)
+    # every row's raw key now sits in the ring at t mod S
+    for t in range(43 - split_at_back, p + 1):
+        np.testing.assert_array_equal(args["ring"][1, t % 8], hist[t])
+
+
+def test_compress_ring_writes_happen_after_pooling_reads():
+    """S = r and a 6-row step: later rows overwrite ring slots the first
+    group still needs; pooling must see the pre-step ring (R14)."""
+    cfg = _cfg(compress_ratio=4, state_size=4)
+    cs = _table()
+    hist = RNG.standard_normal((48, 128))
+    wk = RNG.standard_normal(128) * 0.1
+    start, p_last = 42, 47          # groups 10 (40..43) and 11 (44..47)
+    ring = np.zeros((1, 4, 128))
+    for t in range(38, 42):
+        ring[0, t % 4] = hist[t]
+    rows = p_last - start + 1
+    slots = np.full(rows, -1)
+    slots[43 - start] = 0
+    slots[47 - start] = 1
+    ccache = np.zeros((1, 4, 128))
+    O.compress_stage(cfg, projected_q=None, raw_keys=hist[start:], positions=np.zeros((rows, 3), int),
+                     cos_sin=cs, q_norm_w=np.zeros(128), k_norm_w=wk, ring=ring, ring_pos=None,
+                     ring_block_table=np.array([[0]]), token_to_req=np.zeros(rows, int),
+                     query_start_loc=np.array([0, rows]), logical_positions=np.arange(start, 48),
+                     ccache=ccache, compressed_slots=slots)
+    for slot, g in ((0, 10), (1, 11)):
+        want = O.round_bf16(O.rope_neox(O.gemma_rmsnorm(hist[4 * g:4 * g + 4].mean(0), wk, 1e-6),
+                                        (4 * g,) * 3, cs, 64, (0, 0, 0)))
+        np.testing.assert_array_equal(ccache[0, slot], want)
+    for t in range(44, 48):
+        np.testing.assert_array_equal(ring[0, t % 4], hist[t])
+
+
+def test_prep_query_e4m3_values_are_codes():
+    cfg = _cfg(index_dtype=O.DTYPE_E4M3)
+    q = O.prep_query(cfg, RNG.standard_normal((4, 128)), (9, 9, 9), _table(), np.zeros(128))
+    table = O.e4m3_decode_table()
+    assert np.isin(q, table[~np.isnan(table)]).all()
+
+
+# --------------------------------------------------------------------------
+# Index logits, selection, expand
+# --------------------------------------------------------------------------
+
+def test_index_logits_relu_identity_and_library_check():
+    cfg = _cfg(n_heads=4)
+    q = O.round_e4m3(RNG.standard_normal((4, 128)))
+    k = O.round_e4m3(RNG.standard_normal((50, 128)))
+    s_pos = O.index_logits_row(cfg, q, k)
+    s_neg = O.index_logits_row(cfg, -q, k)
+    scale = 1.0 / (4 * math.sqrt(128))
+    # relu(x) - relu(-x) = x  and  relu(x) + relu(-x) = |x|
+    np.testing.assert_allclose(s_pos - s_neg, (k @ q.sum(0)) * scale, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(s_pos + s_neg, np.abs(k @ q.T).sum(1) * scale, rtol=1e-12, atol=1e-12)
+    lib = torch.relu(torch.einsum("hd,cd->ch", torch.from_numpy(q), torch.from_numpy(k))).sum(1) * scale
+    np.testing.assert_allclose(s_pos, lib.numpy(), rtol=1e-12)
+
+
+def test_index_logits_exact_for_e4m3_inputs():
+    """e4m3 x e4m3 products and their sums are exact in float64 here, so the
+    oracle equals exact rational arithmetic."""
+    cfg = _cfg(n_heads=2)
+    q = O.round_e4m3(RNG.standard_normal((2, 128)))
+    k = O.round_e4m3(RNG.standard_normal((3, 128)))
+    s = O.index_logits_row(cfg, q, k)
+    for c in range(3):
+        tot = Fraction(0)
+        for h in range(2):
+            d = sum(Fraction(q[h, i]) * Fraction(k[c, i]) for i in range(128))
+            tot += max(d, Fraction(0))
+        assert float(tot) / (2 * math.sqrt(128)) == pytest.approx(s[c], rel=1e-15)
+
+
+def test_select_matches_torch_topk_for_distinct_scores():
+    for V, kb in ((100, 16), (5000, 512), (16, 16), (3, 16), (0, 4)):
+        s = RNG.permutation(V).astype(np.float64) / 7.0
+        got = O.select_blocks(s, V, kb)
+        if V <= kb:
+            np.testing.assert_array_equal(got, np.arange(V))
+        else:
+            want = np.sort(torch.topk(torch.from_numpy(s), kb).indices.numpy())
+            np.testing.assert_array_equal(got, want)
+
+
+def test_select_ties_go_to_lower_index():
+    s = np.array([1.0, 5.0, 3.0, 5.0, 3.0, 3.0, 0.0])
+    np.testing.assert_array_equal(O.select_blocks(s, 7, 3), [1, 2, 3])
+    np.testing.assert_array_equal(O.select_blocks(s, 7, 4), [1, 2, 3, 4])
+
+
+def test_expand_golden_rows():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "expand_rows.txt")
+    n = 0
+    for ln in open(path):
+        if not ln.strip() or ln.startswith("#"):
+            continue
+        r, topk, p, blocks, want = ln.split("|")
+        cfg = _cfg(compress_ratio=int(r), token_topk=int(topk))
+        blocks = [int(b) for b in blocks.split(",") if b.strip()]
+        want = [int(v) for v in want.split(",")]
+        np.testing.assert_array_equal(O.expand_row(cfg, blocks, int(p)), want)
+        n += 1
+    assert n >= 4
+
+
+@pytest.mark.parametrize("p", [0, 1, 2, 3, 4, 7, 62, 63, 64, 65, 255, 299, 1000])
+def test_expand_count_closed_form_and_causality(p):
+    cfg = _cfg(compress_ratio=4, token_topk=64)
+    V = O.visible_blocks(p, 4)
+    scores = RNG.standard_normal(V)
+    blocks = O.select_blocks(scores, V, cfg.block_topk)
+    row = O.expand_row(cfg, blocks, p)
+    n = row[-1]
+    assert n == O.expected_count(cfg, p)
+    toks = row[:n]
+    assert len(set(toks.tolist())) == n
+    assert (toks >= 0).all() and (toks <= p).all()
+    assert (row[n:-1] == -1).all()
+    assert len(row) == cfg.token_topk + 4 - 1 + 1
+    if V <= cfg.block_topk:  # everything within budget is selected
+        np.testing.assert_array_equal(np.sort(toks), np.arange(p + 1))
+
+
+# --------------------------------------------------------------------------
+# Sparse GQA
+# --------------------------------------------------------------------------
+
+def _kv_case(L=200, Hq=8, Hkv=2, page=16, D=128):
+    nb = -(-L // page) + 3
+    kv = O.round_bf16(RNG.standard_normal((nb, Hkv, page, 2 * D)))
+    bt = RNG.permutation(nb)[: -(-L // page)]
+    q = O.round_bf16(RNG.standard_normal((Hq, D)))
+    return kv, bt, q
+
+
+def test_sparse_gqa_all_selected_equals_dense_sdpa():
+    L, page, D = 200, 16, 128
+    kv, bt, q = _kv_case(L=L)
+    toks = np.arange(L)
+    got = O.sparse_gqa_row(q, kv, bt, toks, page)
+    blocks = bt[toks // page]
+    k = kv[blocks, :, toks % page, :D]  # [L, Hkv, D]
+    v = kv[blocks, :, toks % page, D:]
+    kk = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(4, 0)  # [Hq, L, D]
+    vv = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(4, 0)
+    ref = F.scaled_dot_product_attention(torch.from_numpy(q)[:, None, :], kk, vv)[:, 0]
+    np.testing.assert_array_equal(got, O.round_bf16(ref.numpy()))
+
+
+def test_sparse_gqa_order_invariant_and_empty():
+    kv, bt, q = _kv_case()
+    toks = RNG.choice(200, size=37, replace=False)
+    a = O.sparse_gqa_row(q, kv, bt, toks, 16)
+    b = O.sparse_gqa_row(q, kv, bt, toks[::-1], 16)
+    np.testing.assert_allclose(a, b, atol=1e-2)  # equal up to bf16 tie rounding
+    assert np.abs(a - b).max() <= 2.0 ** -7 * np.abs(a).max()
+    np.testing.assert_array_equal(O.sparse_gqa_row(q, kv, bt, [], 16), np.zeros_like(q))
+
+
+def test_sparse_gqa_gate_limits():
+    kv, bt, q = _kv_case()
+    toks = np.arange(50)
+    plain = O.sparse_gqa_row(q, kv, bt, toks, 16)
+    np.testing.assert_array_equal(O.sparse_gqa_row(q, kv, bt, toks, 16, np.full(q.shape, 60.0)), plain)
+    np.testing.assert_array_equal(O.sparse_gqa_row(q, kv, bt, toks, 16, np.full(q.shape, -800.0)),
+                                  np.zeros_like(plain))
+    half = O.sparse_gqa_row(q, kv, bt, toks, 16, np.zeros(q.shape))
+    np.testing.assert_array_equal(half, O.round_bf16(plain * 0.5))
+
+
+def test_sparse_gqa_single_token_returns_its_value():
+    kv, bt, q = _kv_case()
+    out = O.sparse_gqa_row(q, kv, bt, [77], 16)
+    v = kv[bt[77 // 16], :, 77 % 16, 128:]
+    np.testing.assert_array_equal(out, np.repeat(v, 4, axis=0))
