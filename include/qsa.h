@@ -1,0 +1,272 @@
+/*
+ * qsa.h -- C ABI of the QSA (Qwen4Exp learned sparse attention) layer step
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * One layer step runs four stages over a batch of query rows:
+ *   1. compress  -- indexer query prep (Gemma RMSNorm, NeoX RoPE / interleaved
+ *                   MRoPE, cast), group pooling into the compressed-key cache
+ *                   and the raw-key ring commit;
+ *   2. logits    -- index scores of each row against its visible compressed
+ *                   keys;
+ *   3. top-k     -- causal, per-request block top-k, expanded into the packed
+ *                   selection buffer;
+ *   4. sparse GQA-- paged grouped-query attention over the selected tokens,
+ *                   with the sigmoid output gate.
+ *
+ * Sources: "vllm.models.qwen4_exp.nvidia.qsa" (QSAIndexer.forward and its
+ * unfused reference path, Qwen4ExpQSAImpl.forward), "vllm.models.qwen4_exp.
+ * nvidia.ops.qsa" (qsa_compress_groups_with_ratio, qsa_sparse_paged_attention,
+ * qsa_store_cache_rows), "indexer_qsa.py" (apply_qsa_rope,
+ * _supports_fused_pre_indexer) and the "FP8 E4M3 KV reader for QSA" patch
+ * (_qsa_sparse_paged_gqa_splitk_kernel).
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor argument is a DEVICE pointer owned by the caller; the
+ *    library never allocates device memory and never frees caller memory.
+ *    Scratch space is passed in as `ws` / `ws_bytes`, sized with
+ *    qsa_workspace_bytes().
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *    legacy default stream) and performs no host synchronisation and no
+ *    device-to-host copy.
+ *  - Host-side validation runs first; on any error nothing is launched and
+ *    the status says why.  Out-of-range page ids, slots or token indices
+ *    that only the device can see are masked (never dereferenced) and
+ *    counted in a device error word that qsa_check_errors() reads.
+ *  - Element types: "bf16" is IEEE bfloat16 stored as uint16; "e4m3" is
+ *    OCP FP8 E4M3FN stored as one byte per element.
+ *  - All index metadata is int32 unless stated; positions and slots are
+ *    int64, as on the pages.
+ *  - rows == 0 is a no-op that returns QSA_OK.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qsa_status {
+  QSA_OK = 0,
+  QSA_ERR_INVALID_ARG = 1,  /* null pointer or inconsistent argument */
+  QSA_ERR_SHAPE = 2,        /* sizes do not fit together */
+  QSA_ERR_DTYPE = 3,        /* unsupported element type */
+  QSA_ERR_UNSUPPORTED = 4,  /* a configuration this build does not run */
+  QSA_ERR_WORKSPACE = 5,    /* ws too small or misaligned */
+  QSA_ERR_CUDA = 6,         /* a CUDA runtime / launch error */
+  QSA_ERR_DEVICE_FAULT = 7  /* device-side masked out-of-range accesses */
+} qsa_status;
+
+enum { QSA_DTYPE_BF16 = 0, QSA_DTYPE_E4M3 = 1 };
+
+/* Indexer configuration ("vllm.models.qwen4_exp.nvidia.qsa", QSAIndexer.__init__:
+ * indexer_n_heads, indexer_head_dim, indexer_budget, indexer_compress_ratio,
+ * rms_norm_eps, the indexer KV dtype; "indexer_qsa.py",
+ * _supports_fused_pre_indexer: NeoX, head_dim 128, rotary_dim 64, one
+ * indexer KV head, compress_ratio a power of two > 1, MRoPE as three
+ * interleaved sections summing to rotary_dim / 2). */
+typedef struct qsa_cfg {
+  int32_t n_heads;          /* H_i, indexer query heads: 8, 16, 32 or 64 */
+  int32_t head_dim;         /* D: must be 128 */
+  int32_t rotary_dim;       /* must be 64 */
+  int32_t compress_ratio;   /* r: power of two, 2..64 */
+  int32_t token_topk;       /* K: multiple of r; K / r blocks are selected */
+  float eps;                /* RMSNorm epsilon */
+  int32_t index_dtype;      /* QSA_DTYPE_BF16 or QSA_DTYPE_E4M3 */
+  int32_t mrope_section[3]; /* all 0: 1-D RoPE; else T,H,W sections, sum 32 */
+  int32_t state_size;       /* S: compressor-state ring slots, >= r */
+  int32_t cpage;            /* compressed keys per compressed-cache page */
+  int32_t max_position;     /* rows of the cos/sin table */
+} qsa_cfg;
+
+/* Main attention configuration ("vllm.models.qwen4_exp.nvidia.qsa",
+ * Qwen4ExpQSAImpl: num_heads, head_size, num_kv_heads; paged KV block size a
+ * multiple of 16). */
+typedef struct qsa_gqa_cfg {
+  int32_t num_q_heads;   /* Hq, a multiple of Hkv with Hq / Hkv == 8 */
+  int32_t num_kv_heads;  /* Hkv */
+  int32_t head_dim;      /* must be 128 */
+  int32_t page_size;     /* tokens per KV block, a multiple of 16 */
+  int32_t num_blocks;    /* KV blocks in the cache */
+} qsa_gqa_cfg;
+
+/*
+ * qsa_compress -- stage 1.
+ * Follows "vllm.models.qwen4_exp.nvidia.qsa", QSAIndexer.forward, unfused
+ * reference path (gemma_rmsnorm(q) -> apply_qsa_rope -> cast;
+ * qsa_compress_groups_with_ratio -> gemma_rmsnorm(pooled) -> RoPE at the
+ * group's first position -> cast -> qsa_store_cache_rows for compressed keys,
+ * raw keys and rope positions) and "vllm.models.qwen4_exp.nvidia.ops.qsa",
+ * qsa_compress_groups_with_ratio (argument shapes and checks).
+ *
+ *  projected_q  [rows, n_heads*D] bf16, row-contiguous; NULL skips query prep
+ *  q_idx        [rows, n_heads, D] index dtype (output); NULL iff projected_q is
+ *  raw_keys     [rows, 1, D] bf16
+ *  positions    [rows, 1, 3] int64 (T, H, W; 1-D RoPE reads component 0)
+ *  cos_sin      [max_position, rotary_dim] fp32: cos in the first half,
+ *               sin in the second
+ *  q_norm_w, k_norm_w  [D] bf16 (Gemma form: scale is 1 + w)
+ *  ring         [ring_blocks, S, 1, D] bf16 compressor-state ring (in/out)
+ *  ring_pos     [ring_blocks, S, 1, 3] int64 (in/out); required with MRoPE,
+ *               must be NULL without it
+ *  ring_block_table [reqs, ring_bt_stride] int32; column 0 is the request's ring
+ *  token_to_req [rows], query_start_loc [reqs + 1], logical_positions [rows]
+ *               (0-based position of the row's token in its request; the
+ *               rows of a request are contiguous and consecutive)
+ *  ccache       [cpages, cpage, 1, D] index dtype compressed-key cache (out)
+ *  compressed_slots [rows] int64: flat slot (page * cpage + offset) where
+ *               the group completed by this row is stored, < 0 for none.
+ *               A row with a slot pools the r tokens ending at its position.
+ * Ring slot of token t of request q: ring_block_table[q, 0] * S + t % S.  All
+ * pooling reads see the ring as it was before the call; afterwards the ring
+ * holds the newest S raw keys of each request.
+ */
+qsa_status qsa_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
+                        const void* raw_keys, const int64_t* positions,
+                        const float* cos_sin, const void* q_norm_w,
+                        const void* k_norm_w, void* ring, int32_t ring_blocks,
+                        int64_t* ring_pos, const int32_t* ring_block_table,
+                        int32_t ring_bt_stride, const int32_t* token_to_req,
+                        const int32_t* query_start_loc,
+                        const int32_t* logical_positions, void* ccache,
+                        int32_t cpages, const int64_t* compressed_slots,
+                        int32_t rows, int32_t reqs, void* stream);
+
+/*
+ * qsa_index_logits -- stage 2.
+ * Follows "vllm.models.qwen4_exp.nvidia.qsa", QSAIndexer.forward
+ * (qsa_select_paged_decode / qsa_select_paged_prefill score the indexer
+ * query against the paged compressed-key cache through its block table; the
+ * selection is weight-free).  Score of row i and compressed key c < V(p_i),
+ * V(p) = floor((p + 1) / r):
+ *     logits[i, c] = (1 / (n_heads * sqrt(D))) * sum_h max(0, q_idx[i,h] . k_c)
+ * with exact products and fp32 accumulation (tcgen05 MMA).
+ *  q_idx        [rows, n_heads, D] index dtype
+ *  ccache       [cpages, cpage, 1, D] index dtype
+ *  cblock_table [reqs, cbt_stride] int32: key c of request q is at page
+ *               cblock_table[q, c / cpage], offset c % cpage
+ *  logits       [rows, ld] fp32 (out); entries c >= V(p_i) are not written
+ *  max_visible  upper bound of V(p) over the rows (ld >= max_visible)
+ *  ws           scratch (row-group table), qsa_workspace_bytes() bytes
+ */
+qsa_status qsa_index_logits(const qsa_cfg* cfg, const void* q_idx,
+                            const void* ccache, int32_t cpages,
+                            const int32_t* cblock_table, int32_t cbt_stride,
+                            const int32_t* token_to_req,
+                            const int32_t* query_start_loc,
+                            const int32_t* logical_positions, float* logits,
+                            int64_t ld, int32_t max_visible, int32_t rows,
+                            int32_t reqs, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/*
+ * qsa_topk -- stage 3 (block top-k and expand).
+ * Follows "vllm.models.qwen4_exp.nvidia.qsa", QSAIndexer.forward
+ * (block_indices of token_topk / compress_ratio columns, then
+ * expand_qsa_block_indices) and the packed_output_width docstring.
+ * For each row with V = V(p) visible blocks: the K_b = token_topk / r blocks
+ * with the highest logits (ties to the lower block; all blocks if V <= K_b),
+ * expanded in ascending order into their r tokens each, followed by the tail
+ * tokens V*r .. p.  packed[i, 0 .. W-1] holds request-relative token indices
+ * padded with -1; packed[i, W] holds their count, W = token_topk + r - 1.
+ *  logits [rows, ld] fp32 (read only where c < V)
+ *  packed [rows, W + 1] int32 (out)
+ */
+qsa_status qsa_topk(const qsa_cfg* cfg, const float* logits, int64_t ld,
+                    int32_t max_visible, const int32_t* logical_positions,
+                    int32_t* packed, int32_t rows, void* stream);
+
+/*
+ * qsa_sparse_gqa -- stage 4.
+ * Follows "vllm.models.qwen4_exp.nvidia.ops.qsa", qsa_sparse_paged_attention
+ * and the patch's _qsa_sparse_paged_gqa_splitk_kernel: for row i and query
+ * head h (KV head h / (Hq / Hkv)), attention with scale D^-1/2 over the
+ * packed[i, 0 .. n-1] tokens (n = packed[i, packed_width - 1]), zero when
+ * n == 0, split-KV partials in fp32 merged by log-sum-exp, then
+ * out = bf16(bf16(attn) * sigmoid(gate)) (or bf16(attn) when gate is NULL).
+ *  q      [rows, Hq, D] bf16
+ *  kv     [num_blocks, Hkv, page_size, 2*D] bf16 (K in [..., :D], V in [..., D:])
+ *  block_table [reqs, bt_stride] int32: token t of request q is in block
+ *         block_table[q, t / page_size], offset t % page_size
+ *  packed [rows, packed_width] int32; token_to_req [rows]
+ *  gate   [rows, Hq, D] bf16 or NULL;  out [rows, Hq, D] bf16
+ *  ws     scratch (split-KV partials), qsa_workspace_bytes() bytes
+ */
+qsa_status qsa_sparse_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
+                          const int32_t* block_table, int32_t bt_stride,
+                          const int32_t* packed, int32_t packed_width,
+                          const int32_t* token_to_req, const void* gate,
+                          void* out, int32_t rows, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* Arguments of one fused layer step (all device pointers; meanings as in the
+ * stage calls above). */
+typedef struct qsa_step_args {
+  int32_t rows, reqs;
+  int32_t max_visible;              /* upper bound of V(p) over the rows */
+  const void* projected_q;          /* [rows, n_heads*D] bf16 */
+  const void* raw_keys;             /* [rows, 1, D] bf16 */
+  const int64_t* positions;         /* [rows, 1, 3] int64 */
+  const float* cos_sin;             /* [max_position, rotary_dim] fp32 */
+  const void* q_norm_w;             /* [D] bf16 */
+  const void* k_norm_w;             /* [D] bf16 */
+  void* ring;                       /* [ring_blocks, S, 1, D] bf16 */
+  int32_t ring_blocks;
+  int64_t* ring_pos;                /* [ring_blocks, S, 1, 3] or NULL */
+  const int32_t* ring_block_table;  /* [reqs, ring_bt_stride] */
+  int32_t ring_bt_stride;
+  void* ccache;                     /* [cpages, cpage, 1, D] index dtype */
+  int32_t cpages;
+  const int32_t* cblock_table;      /* [reqs, cbt_stride] */
+  int32_t cbt_stride;
+  const int64_t* compressed_slots;  /* [rows] */
+  const int32_t* token_to_req;      /* [rows] */
+  const int32_t* query_start_loc;   /* [reqs + 1] */
+  const int32_t* logical_positions; /* [rows] */
+  int32_t* packed;                  /* [rows, token_topk + r] (out, or in with skip_topk) */
+  const void* q;                    /* [rows, Hq, D] bf16 */
+  const void* kv;                   /* [num_blocks, Hkv, page, 2D] bf16 */
+  const int32_t* block_table;       /* [reqs, bt_stride] */
+  int32_t bt_stride;
+  const void* gate;                 /* [rows, Hq, D] bf16 or NULL */
+  void* out;                        /* [rows, Hq, D] bf16 */
+} qsa_step_args;
+
+/*
+ * qsa_layer_step -- stages 1 to 4 in order on one stream.
+ * Follows "vllm.models.qwen4_exp.nvidia.qsa", Qwen4ExpQSAAttention._run_qsa
+ * and QSAIndexer.forward.  With skip_topk != 0 (MTP steps after step 0,
+ * QSAIndexer.skip_topk) stage 1 still updates the ring and the compressed
+ * cache, stages 2-3 are skipped and stage 4 reads the packed buffer as
+ * given; skip_topk with a NULL packed buffer is QSA_ERR_INVALID_ARG ("QSA
+ * top-k reuse requires an output buffer").
+ */
+qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg,
+                          const qsa_step_args* args, int32_t skip_topk,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Scratch bytes needed by qsa_layer_step (and enough for every stage call)
+ * for `rows` rows, `reqs` requests and V(p) <= max_visible.  The workspace
+ * must be 256-byte aligned.  Returns 0 for invalid configurations. */
+size_t qsa_workspace_bytes(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg,
+                           int32_t rows, int32_t reqs, int32_t max_visible);
+
+/* Static description of a status code. */
+const char* qsa_status_string(qsa_status status);
+
+/* Synchronises the current device, reads and clears the device error word
+ * (count of masked out-of-range pages, slots or tokens since the last
+ * call, and whether a bounded device-side wait gave up).  Returns
+ * QSA_ERR_DEVICE_FAULT when it was non-zero, QSA_ERR_CUDA on a CUDA error,
+ * else QSA_OK.  `count` may be NULL. */
+qsa_status qsa_check_errors(int64_t* count);
+
+/* Library version string. */
+const char* qsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QSA_H */

@@ -1,0 +1,487 @@
+// C ABI of the QSA layer step (declared in include/qsa.h): host-side
+// validation, workspace layout, TMA descriptor encoding and kernel launch
+// order.  Nothing here allocates device memory.
+#include <mutex>
+
+#include "qsa.h"
+#include "qsa_device.cuh"
+#include "qsa_kernels.h"
+
+namespace qsa {
+namespace {
+
+__device__ unsigned long long g_error_word;
+
+constexpr int kMaxDevices = 64;
+unsigned long long* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mu;
+
+// Device address of the error word for the current device (resolved once per
+// device with that device current).
+unsigned long long* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned long long*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over [outer, 128 elements] rows with a 128-byte-wide box of
+// `box_rows` rows, 128-byte swizzle, zero fill out of bounds.
+bool encode_rows_map(CUtensorMap* map, const void* base, int elem_bytes, long long outer,
+                     int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const CUtensorMapDataType dt =
+      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(128 * elem_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+qsa_status check_cfg(const qsa_cfg* c) {
+  if (c == nullptr) return QSA_ERR_INVALID_ARG;
+  if (c->head_dim != 128 || c->rotary_dim != 64) return QSA_ERR_UNSUPPORTED;
+  if (!(c->n_heads == 8 || c->n_heads == 16 || c->n_heads == 32 || c->n_heads == 64))
+    return QSA_ERR_UNSUPPORTED;
+  if (!pow2(c->compress_ratio) || c->compress_ratio < 2 || c->compress_ratio > 64)
+    return QSA_ERR_UNSUPPORTED;
+  if (c->token_topk <= 0 || c->token_topk % c->compress_ratio != 0) return QSA_ERR_INVALID_ARG;
+  if (!(c->eps >= 0.f)) return QSA_ERR_INVALID_ARG;
+  if (c->index_dtype != QSA_DTYPE_BF16 && c->index_dtype != QSA_DTYPE_E4M3) return QSA_ERR_DTYPE;
+  const int* s = c->mrope_section;
+  const bool any = s[0] || s[1] || s[2];
+  if (any && (s[0] < 0 || s[1] < 0 || s[2] < 0 || s[0] + s[1] + s[2] != 32))
+    return QSA_ERR_UNSUPPORTED;
+  if (c->state_size < c->compress_ratio) return QSA_ERR_SHAPE;
+  if (!pow2(c->cpage) || c->cpage > 128) return QSA_ERR_UNSUPPORTED;
+  if (c->max_position < 1) return QSA_ERR_INVALID_ARG;
+  return QSA_OK;
+}
+
+qsa_status check_gcfg(const qsa_gqa_cfg* g) {
+  if (g == nullptr) return QSA_ERR_INVALID_ARG;
+  if (g->head_dim != 128) return QSA_ERR_UNSUPPORTED;
+  if (g->num_kv_heads < 1 || g->num_q_heads != 8 * g->num_kv_heads) return QSA_ERR_UNSUPPORTED;
+  if (g->page_size < 16 || g->page_size % 16 != 0) return QSA_ERR_SHAPE;
+  if (g->num_blocks < 1) return QSA_ERR_SHAPE;
+  return QSA_OK;
+}
+
+int elem_bytes(const qsa_cfg* c) { return c->index_dtype == QSA_DTYPE_E4M3 ? 1 : 2; }
+
+// Rows per logits row group and the padded MMA N it implies.
+void logits_grouping(const qsa_cfg* c, int rows, int reqs, int* R, int* npad) {
+  const int max_r = 256 / c->n_heads;
+  int avg = reqs > 0 ? (rows + reqs - 1) / reqs : 1;
+  int r = 1;
+  while (r < avg && r < max_r) r <<= 1;
+  if (r > max_r) r = max_r;
+  int n = r * c->n_heads;
+  int np = 32;
+  while (np < n) np <<= 1;
+  *R = r;
+  *npad = np;
+}
+
+int max_groups_for(int rows, int reqs, int R) {
+  long long a = static_cast<long long>(rows) / R + reqs;
+  if (a > rows) a = rows;
+  return static_cast<int>(a < 1 ? 1 : a);
+}
+
+long long logits_ld(int max_visible) { return (static_cast<long long>(max_visible) + 3) / 4 * 4; }
+
+size_t logits_ws_bytes(int rows, int reqs, const qsa_cfg* c) {
+  int R, np;
+  logits_grouping(c, rows, reqs, &R, &np);
+  return align256(static_cast<size_t>(max_groups_for(rows, reqs, R)) * sizeof(int4)) + 256;
+}
+
+size_t gqa_ws_bytes(const qsa_gqa_cfg* g, int rows, int packed_width) {
+  const int s = gqa_num_splits(rows, g->num_kv_heads, packed_width);
+  if (s == 1) return 0;
+  const size_t po = static_cast<size_t>(s) * rows * g->num_q_heads * 128 * sizeof(float);
+  const size_t pl = static_cast<size_t>(s) * rows * g->num_q_heads * sizeof(float);
+  return align256(po) + align256(pl);
+}
+
+qsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA; }
+
+size_t topk_limit_bytes() { return 220 * 1024; }
+
+qsa_status do_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
+                       const void* raw_keys, const int64_t* positions, const float* cos_sin,
+                       const void* q_norm_w, const void* k_norm_w, void* ring, int32_t ring_blocks,
+                       int64_t* ring_pos, const int32_t* ring_block_table, int32_t ring_bt_stride,
+                       const int32_t* token_to_req, const int32_t* query_start_loc,
+                       const int32_t* logical_positions, void* ccache, int32_t cpages,
+                       const int64_t* compressed_slots, int32_t rows, int32_t reqs,
+                       cudaStream_t stream) {
+  qsa_status st = check_cfg(cfg);
+  if (st != QSA_OK) return st;
+  if (rows < 0 || reqs < 0) return QSA_ERR_SHAPE;
+  if (rows == 0) return QSA_OK;
+  if (reqs < 1 || ring_blocks < 1 || cpages < 1 || ring_bt_stride < 1) return QSA_ERR_SHAPE;
+  if ((projected_q == nullptr) != (q_idx == nullptr)) return QSA_ERR_INVALID_ARG;
+  if (!raw_keys || !positions || !cos_sin || !q_norm_w || !k_norm_w || !ring ||
+      !ring_block_table || !token_to_req || !query_start_loc || !logical_positions || !ccache ||
+      !compressed_slots)
+    return QSA_ERR_INVALID_ARG;
+  const bool mrope = cfg->mrope_section[0] || cfg->mrope_section[1] || cfg->mrope_section[2];
+  if (mrope != (ring_pos != nullptr)) return QSA_ERR_INVALID_ARG;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(raw_keys) | reinterpret_cast<uintptr_t>(ring) |
+                        reinterpret_cast<uintptr_t>(ccache) | reinterpret_cast<uintptr_t>(q_norm_w) |
+                        reinterpret_cast<uintptr_t>(k_norm_w) |
+                        reinterpret_cast<uintptr_t>(projected_q) | reinterpret_cast<uintptr_t>(q_idx);
+  if (a16 & 15) return QSA_ERR_INVALID_ARG;
+
+  CompressParams p{};
+  p.projected_q = static_cast<const uint16_t*>(projected_q);
+  p.q_idx = q_idx;
+  p.raw_keys = static_cast<const uint16_t*>(raw_keys);
+  p.positions = positions;
+  p.cos_sin = cos_sin;
+  p.q_norm_w = static_cast<const uint16_t*>(q_norm_w);
+  p.k_norm_w = static_cast<const uint16_t*>(k_norm_w);
+  p.ring = static_cast<uint16_t*>(ring);
+  p.ring_pos = ring_pos;
+  p.ring_bt = ring_block_table;
+  p.token_to_req = token_to_req;
+  p.qsl = query_start_loc;
+  p.logical = logical_positions;
+  p.ccache = ccache;
+  p.slots = compressed_slots;
+  p.ring_blocks = ring_blocks;
+  p.ring_bt_stride = ring_bt_stride;
+  p.cpages = cpages;
+  p.cpage = cfg->cpage;
+  p.rows = rows;
+  p.reqs = reqs;
+  p.n_heads = cfg->n_heads;
+  p.ratio = cfg->compress_ratio;
+  p.S = cfg->state_size;
+  p.max_pos = cfg->max_position;
+  p.index_dtype = cfg->index_dtype;
+  p.mrope = mrope ? 1 : 0;
+  p.sec_h = cfg->mrope_section[1];
+  p.sec_w = cfg->mrope_section[2];
+  p.eps = cfg->eps;
+  p.err = error_word();
+  if (p.err == nullptr) return QSA_ERR_CUDA;
+  st = cuda_status(launch_compress(p, stream));
+  if (st != QSA_OK) return st;
+  return cuda_status(launch_ring_commit(p, stream));
+}
+
+qsa_status do_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache, int32_t cpages,
+                     const int32_t* cblock_table, int32_t cbt_stride, const int32_t* token_to_req,
+                     const int32_t* query_start_loc, const int32_t* logical_positions,
+                     float* logits, int64_t ld, int32_t max_visible, int32_t rows, int32_t reqs,
+                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+  qsa_status st = check_cfg(cfg);
+  if (st != QSA_OK) return st;
+  if (rows < 0 || reqs < 0 || max_visible < 0) return QSA_ERR_SHAPE;
+  if (rows == 0 || max_visible == 0) return QSA_OK;
+  if (reqs < 1 || cpages < 1 || cbt_stride < 1 || ld < max_visible) return QSA_ERR_SHAPE;
+  if (!q_idx || !ccache || !cblock_table || !token_to_req || !query_start_loc ||
+      !logical_positions || !logits || !ws)
+    return QSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_idx) | reinterpret_cast<uintptr_t>(ccache)) & 15)
+    return QSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & 255) return QSA_ERR_WORKSPACE;
+  if (ws_bytes < logits_ws_bytes(rows, reqs, cfg)) return QSA_ERR_WORKSPACE;
+  (void)token_to_req;
+
+  int R, npad;
+  logits_grouping(cfg, rows, reqs, &R, &npad);
+  const int max_groups = max_groups_for(rows, reqs, R);
+  const int eb = elem_bytes(cfg);
+  LogitsParams p{};
+  p.cblock_table = cblock_table;
+  p.logical = logical_positions;
+  p.qsl = query_start_loc;
+  p.groups = static_cast<int4*>(ws);
+  p.group_count = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) +
+                                         align256(static_cast<size_t>(max_groups) * sizeof(int4)));
+  p.logits = logits;
+  p.ccache = static_cast<const uint8_t*>(ccache);
+  p.ld = ld;
+  p.cbt_stride = cbt_stride;
+  p.cpages = cpages;
+  p.cpage = cfg->cpage;
+  p.reqs = reqs;
+  p.rows_per_group = R;
+  p.max_groups = max_groups;
+  p.n_heads = cfg->n_heads;
+  p.ratio = cfg->compress_ratio;
+  p.scale = 1.0f / (static_cast<float>(cfg->n_heads) * sqrtf(128.0f));
+  p.manual = cfg->cpage < 8 ? 1 : 0;
+  p.row_bytes = 128 * eb;
+  p.err = error_word();
+  if (p.err == nullptr) return QSA_ERR_CUDA;
+
+  const int max_tiles = (max_visible + 127) / 128;
+  // Spread the key tiles so that about four CTAs per SM are available.
+  const long long work = static_cast<long long>(max_groups) * max_tiles;
+  long long tpc = (work + 4 * 152 - 1) / (4 * 152);
+  if (tpc < 2) tpc = 2;
+  if (tpc > max_tiles) tpc = max_tiles;
+  p.tiles_per_cta = static_cast<int>(tpc);
+  const int chunks = static_cast<int>((max_tiles + tpc - 1) / tpc);
+
+  CUtensorMap tq, tk;
+  if (!encode_rows_map(&tq, q_idx, eb, static_cast<long long>(rows) * cfg->n_heads, npad))
+    return QSA_ERR_CUDA;
+  const int kbox = p.manual ? 8 : cfg->cpage;
+  if (!encode_rows_map(&tk, ccache, eb, static_cast<long long>(cpages) * cfg->cpage, kbox))
+    return QSA_ERR_CUDA;
+  st = cuda_status(launch_logits_plan(p, stream));
+  if (st != QSA_OK) return st;
+  return cuda_status(
+      launch_index_logits(p, tq, tk, cfg->index_dtype, npad, max_groups, chunks, stream));
+}
+
+qsa_status do_topk(const qsa_cfg* cfg, const float* logits, int64_t ld, int32_t max_visible,
+                   const int32_t* logical_positions, int32_t* packed, int32_t rows,
+                   cudaStream_t stream) {
+  qsa_status st = check_cfg(cfg);
+  if (st != QSA_OK) return st;
+  if (rows < 0 || max_visible < 0) return QSA_ERR_SHAPE;
+  if (rows == 0) return QSA_OK;
+  if (!logical_positions || !packed) return QSA_ERR_INVALID_ARG;
+  const int kb = cfg->token_topk / cfg->compress_ratio;
+  if (max_visible > kb && (!logits || ld < max_visible)) return QSA_ERR_INVALID_ARG;
+  if (topk_smem_bytes(max_visible, kb) > topk_limit_bytes()) return QSA_ERR_UNSUPPORTED;
+  TopkParams p{};
+  p.logits = logits;
+  p.ld = ld;
+  p.logical = logical_positions;
+  p.packed = packed;
+  p.rows = rows;
+  p.ratio = cfg->compress_ratio;
+  p.token_topk = cfg->token_topk;
+  p.max_visible = max_visible;
+  p.err = error_word();
+  if (p.err == nullptr) return QSA_ERR_CUDA;
+  return cuda_status(launch_topk(p, stream));
+}
+
+qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
+                  const int32_t* block_table, int32_t bt_stride, const int32_t* packed,
+                  int32_t packed_width, const int32_t* token_to_req, const void* gate, void* out,
+                  int32_t rows, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  qsa_status st = check_gcfg(gcfg);
+  if (st != QSA_OK) return st;
+  if (rows < 0) return QSA_ERR_SHAPE;
+  if (rows == 0) return QSA_OK;
+  if (packed_width < 2 || bt_stride < 1) return QSA_ERR_SHAPE;
+  if (!q || !kv || !block_table || !packed || !token_to_req || !out) return QSA_ERR_INVALID_ARG;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv) |
+                        reinterpret_cast<uintptr_t>(gate) | reinterpret_cast<uintptr_t>(out);
+  if (a16 & 15) return QSA_ERR_INVALID_ARG;
+  GqaParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv = static_cast<const uint16_t*>(kv);
+  p.block_table = block_table;
+  p.packed = packed;
+  p.token_to_req = token_to_req;
+  p.gate = static_cast<const uint16_t*>(gate);
+  p.out = static_cast<uint16_t*>(out);
+  p.bt_stride = bt_stride;
+  p.packed_width = packed_width;
+  p.rows = rows;
+  p.hq = gcfg->num_q_heads;
+  p.hkv = gcfg->num_kv_heads;
+  p.page = gcfg->page_size;
+  p.num_blocks = gcfg->num_blocks;
+  p.splits = gqa_num_splits(rows, gcfg->num_kv_heads, packed_width);
+  if (p.splits > 1) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255)) return QSA_ERR_WORKSPACE;
+    if (ws_bytes < gqa_ws_bytes(gcfg, rows, packed_width)) return QSA_ERR_WORKSPACE;
+    const size_t po = static_cast<size_t>(p.splits) * rows * p.hq * 128 * sizeof(float);
+    p.part_o = static_cast<float*>(ws);
+    p.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(po));
+  }
+  p.err = error_word();
+  if (p.err == nullptr) return QSA_ERR_CUDA;
+  return cuda_status(launch_sparse_gqa(p, stream));
+}
+
+// Layer-step workspace regions.
+struct StepLayout {
+  size_t q_idx, logits, logits_ws, gqa_ws, total;
+  long long ld;
+};
+
+bool step_layout(const qsa_cfg* c, const qsa_gqa_cfg* g, int rows, int reqs, int max_visible,
+                 StepLayout* L) {
+  if (check_cfg(c) != QSA_OK || check_gcfg(g) != QSA_OK) return false;
+  if (rows < 0 || reqs < 0 || max_visible < 0) return false;
+  const int pw = c->token_topk + c->compress_ratio;
+  L->ld = logits_ld(max_visible);
+  size_t off = 0;
+  L->q_idx = off;
+  off += align256(static_cast<size_t>(rows) * c->n_heads * 128 * elem_bytes(c));
+  L->logits = off;
+  off += align256(static_cast<size_t>(rows) * L->ld * sizeof(float));
+  L->logits_ws = off;
+  off += logits_ws_bytes(rows, reqs, c);
+  L->gqa_ws = off;
+  off += gqa_ws_bytes(g, rows, pw);
+  L->total = off + 256;
+  return true;
+}
+
+}  // namespace
+}  // namespace qsa
+
+using namespace qsa;
+
+extern "C" {
+
+qsa_status qsa_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
+                        const void* raw_keys, const int64_t* positions, const float* cos_sin,
+                        const void* q_norm_w, const void* k_norm_w, void* ring,
+                        int32_t ring_blocks, int64_t* ring_pos,
+                        const int32_t* ring_block_table, int32_t ring_bt_stride,
+                        const int32_t* token_to_req, const int32_t* query_start_loc,
+                        const int32_t* logical_positions, void* ccache, int32_t cpages,
+                        const int64_t* compressed_slots, int32_t rows, int32_t reqs,
+                        void* stream) {
+  return do_compress(cfg, projected_q, q_idx, raw_keys, positions, cos_sin, q_norm_w, k_norm_w,
+                     ring, ring_blocks, ring_pos, ring_block_table, ring_bt_stride, token_to_req,
+                     query_start_loc, logical_positions, ccache, cpages, compressed_slots, rows,
+                     reqs, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_index_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache,
+                            int32_t cpages, const int32_t* cblock_table, int32_t cbt_stride,
+                            const int32_t* token_to_req, const int32_t* query_start_loc,
+                            const int32_t* logical_positions, float* logits, int64_t ld,
+                            int32_t max_visible, int32_t rows, int32_t reqs, void* ws,
+                            size_t ws_bytes, void* stream) {
+  return do_logits(cfg, q_idx, ccache, cpages, cblock_table, cbt_stride, token_to_req,
+                   query_start_loc, logical_positions, logits, ld, max_visible, rows, reqs, ws,
+                   ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_topk(const qsa_cfg* cfg, const float* logits, int64_t ld, int32_t max_visible,
+                    const int32_t* logical_positions, int32_t* packed, int32_t rows,
+                    void* stream) {
+  return do_topk(cfg, logits, ld, max_visible, logical_positions, packed, rows,
+                 static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_sparse_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
+                          const int32_t* block_table, int32_t bt_stride, const int32_t* packed,
+                          int32_t packed_width, const int32_t* token_to_req, const void* gate,
+                          void* out, int32_t rows, void* ws, size_t ws_bytes, void* stream) {
+  return do_gqa(gcfg, q, kv, block_table, bt_stride, packed, packed_width, token_to_req, gate, out,
+                rows, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa_step_args* a,
+                          int32_t skip_topk, void* ws, size_t ws_bytes, void* stream) {
+  if (a == nullptr) return QSA_ERR_INVALID_ARG;
+  qsa_status st = check_cfg(cfg);
+  if (st != QSA_OK) return st;
+  st = check_gcfg(gcfg);
+  if (st != QSA_OK) return st;
+  if (a->rows < 0 || a->reqs < 0) return QSA_ERR_SHAPE;
+  if (a->packed == nullptr) return QSA_ERR_INVALID_ARG;
+  if (a->rows == 0) return QSA_OK;
+  StepLayout L;
+  if (!step_layout(cfg, gcfg, a->rows, a->reqs, a->max_visible, &L)) return QSA_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255)) return QSA_ERR_WORKSPACE;
+  if (ws_bytes < L.total) return QSA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* q_idx = skip_topk ? nullptr : w + L.q_idx;
+  st = do_compress(cfg, skip_topk ? nullptr : a->projected_q, q_idx, a->raw_keys, a->positions,
+                   a->cos_sin, a->q_norm_w, a->k_norm_w, a->ring, a->ring_blocks, a->ring_pos,
+                   a->ring_block_table, a->ring_bt_stride, a->token_to_req, a->query_start_loc,
+                   a->logical_positions, a->ccache, a->cpages, a->compressed_slots, a->rows,
+                   a->reqs, s);
+  if (st != QSA_OK) return st;
+  const int pw = cfg->token_topk + cfg->compress_ratio;
+  if (!skip_topk) {
+    float* logits = reinterpret_cast<float*>(w + L.logits);
+    st = do_logits(cfg, q_idx, a->ccache, a->cpages, a->cblock_table, a->cbt_stride,
+                   a->token_to_req, a->query_start_loc, a->logical_positions, logits, L.ld,
+                   a->max_visible, a->rows, a->reqs, w + L.logits_ws, L.gqa_ws - L.logits_ws, s);
+    if (st != QSA_OK) return st;
+    st = do_topk(cfg, logits, L.ld, a->max_visible, a->logical_positions, a->packed, a->rows, s);
+    if (st != QSA_OK) return st;
+  }
+  return do_gqa(gcfg, a->q, a->kv, a->block_table, a->bt_stride, a->packed, pw, a->token_to_req,
+                a->gate, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s);
+}
+
+size_t qsa_workspace_bytes(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t rows,
+                           int32_t reqs, int32_t max_visible) {
+  StepLayout L;
+  if (!step_layout(cfg, gcfg, rows, reqs, max_visible, &L)) return 0;
+  return L.total;
+}
+
+const char* qsa_status_string(qsa_status s) {
+  switch (s) {
+    case QSA_OK: return "ok";
+    case QSA_ERR_INVALID_ARG: return "invalid argument (null pointer, misaligned or inconsistent)";
+    case QSA_ERR_SHAPE: return "sizes do not fit together";
+    case QSA_ERR_DTYPE: return "unsupported element type";
+    case QSA_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case QSA_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case QSA_ERR_CUDA: return "CUDA runtime or launch error";
+    case QSA_ERR_DEVICE_FAULT: return "device reported masked out-of-range accesses or a wait timeout";
+  }
+  return "unknown status";
+}
+
+qsa_status qsa_check_errors(int64_t* count) {
+  if (count) *count = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return QSA_ERR_CUDA;
+  unsigned long long* p = error_word();
+  if (p == nullptr) return QSA_ERR_CUDA;
+  unsigned long long v = 0, zero = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QSA_ERR_CUDA;
+  if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  if (count) *count = static_cast<int64_t>(v);
+  return v ? QSA_ERR_DEVICE_FAULT : QSA_OK;
+}
+
+const char* qsa_version(void) { return "qsa-gb300 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

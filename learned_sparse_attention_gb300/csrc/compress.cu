@@ -1,0 +1,229 @@
+// Stage 1 of the QSA layer step: indexer query prep, group pooling into the
+// compressed-key cache and the compressor-state ring commit.
+//
+// Follows "vllm.models.qwen4_exp.nvidia.qsa", QSAIndexer.forward (unfused
+// reference path: gemma_rmsnorm -> apply_qsa_rope -> cast for the query;
+// qsa_compress_groups_with_ratio -> gemma_rmsnorm -> RoPE at the group's first
+// position -> cast -> qsa_store_cache_rows for the compressed key, the raw key
+// and the rope position) and "indexer_qsa.py", apply_qsa_rope (NeoX pairs
+// (i, i + rotary_dim/2), cos|sin halves of the caller's table, interleaved
+// MRoPE).  The norm, rotation and cast are fused into one pass in fp32 with a
+// single rounding to the indexer dtype.
+//
+// Layout of the work: one CTA per row, 128 threads = 8 half-warps; a
+// half-warp owns one 128-dim head vector, each lane 8 consecutive dims
+// (one 16-byte load).  RoPE partners (i, i + 32) sit 4 lanes apart.
+#include "qsa_device.cuh"
+#include "qsa_kernels.h"
+
+namespace qsa {
+namespace {
+
+constexpr int kD = 128;
+
+__device__ __forceinline__ int mrope_component(int i, int mrope, int sec_h, int sec_w) {
+  if (!mrope) return 0;
+  if (i % 3 == 1 && i < 3 * sec_h) return 1;
+  if (i % 3 == 2 && i < 3 * sec_w) return 2;
+  return 0;
+}
+
+__device__ __forceinline__ void load8_bf16(const uint16_t* src, float (&x)[8]) {
+  const uint4 v = *reinterpret_cast<const uint4*>(src);
+  x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x);
+  x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+  x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z);
+  x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+}
+
+// cos/sin of the 8 frequencies this lane touches, at a 3-component position.
+__device__ __forceinline__ void rope_coeffs(const CompressParams& P, int lane16,
+                                            const int64_t (&pos)[3], float (&c)[8],
+                                            float (&s)[8]) {
+  const int fbase = 8 * (lane16 & 3);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int i = fbase + e;
+    int64_t pp = pos[mrope_component(i, P.mrope, P.sec_h, P.sec_w)];
+    if (pp < 0 || pp >= P.max_pos) {
+      if (lane16 == 0 && e == 0) flag_error(P.err);
+      pp = pp < 0 ? 0 : P.max_pos - 1;
+    }
+    const float* row = P.cos_sin + pp * 64;
+    c[e] = row[i];
+    s[e] = row[32 + i];
+  }
+}
+
+// Gemma RMSNorm over the half-warp's 128 dims, then NeoX rotation of dims
+// 0..63, in place on x (this lane's 8 dims).
+__device__ __forceinline__ void norm_rope(float (&x)[8], const float (&w1)[8], float eps,
+                                          int lane16, const float (&c)[8], const float (&s)[8]) {
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float inv = rsqrtf(ss * (1.0f / kD) + eps);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) x[e] = x[e] * inv * w1[e];
+  float partner[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) partner[e] = __shfl_xor_sync(0xffffffffu, x[e], 4);
+  if (lane16 < 4) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = x[e] * c[e] - partner[e] * s[e];
+  } else if (lane16 < 8) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = x[e] * c[e] + partner[e] * s[e];
+  }
+}
+
+template <int IDT>
+__device__ __forceinline__ void store8(void* base, long long elem_off, const float (&x)[8]) {
+  if (IDT == 1) {
+    uint2 v;
+    v.x = static_cast<uint32_t>(f32x2_to_e4m3x2(x[0], x[1])) |
+          (static_cast<uint32_t>(f32x2_to_e4m3x2(x[2], x[3])) << 16);
+    v.y = static_cast<uint32_t>(f32x2_to_e4m3x2(x[4], x[5])) |
+          (static_cast<uint32_t>(f32x2_to_e4m3x2(x[6], x[7])) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(base) + elem_off) = v;
+  } else {
+    uint4 v;
+    v.x = pack_bf16x2(x[0], x[1]);
+    v.y = pack_bf16x2(x[2], x[3]);
+    v.z = pack_bf16x2(x[4], x[5]);
+    v.w = pack_bf16x2(x[6], x[7]);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + elem_off) = v;
+  }
+}
+
+template <int IDT>
+__global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
+  const int row = blockIdx.x;
+  const int hw = threadIdx.x >> 4;       // half-warp 0..7
+  const int lane16 = threadIdx.x & 15;   // dims 8*lane16 .. +7
+  const int req = P.token_to_req[row];
+  const int p = P.logical[row];
+  if (req < 0 || req >= P.reqs) {
+    if (threadIdx.x == 0) flag_error(P.err);
+    return;
+  }
+
+  // ---- indexer query: every head of this row
+  if (P.projected_q != nullptr) {
+    int64_t pos[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+      pos[k] = P.positions[static_cast<long long>(row) * 3 + (P.mrope ? k : 0)];
+    float c[8], s[8], w1[8];
+    rope_coeffs(P, lane16, pos, c, s);
+    load8_bf16(P.q_norm_w + 8 * lane16, w1);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w1[e] += 1.0f;
+    for (int h = hw; h < P.n_heads; h += 8) {
+      const long long off = (static_cast<long long>(row) * P.n_heads + h) * kD + 8 * lane16;
+      float x[8];
+      load8_bf16(P.projected_q + off, x);
+      norm_rope(x, w1, P.eps, lane16, c, s);
+      store8<IDT>(P.q_idx, off, x);
+    }
+  }
+
+  // ---- group completed by this row: pool, norm, rotate, cast, store.
+  // Warp 0 runs it; both of its half-warps compute the same key (the
+  // shuffles stay inside a half-warp) and half-warp 0 stores it.
+  const long long slot = P.slots[row];
+  if (slot < 0 || (threadIdx.x >> 5) != 0) return;
+  const int r = P.ratio;
+  const int first_row = P.qsl[req];
+  const int step_start = P.logical[first_row];
+  const int ring_block = P.ring_bt[static_cast<long long>(req) * P.ring_bt_stride];
+  const long long nslots = static_cast<long long>(P.cpages) * P.cpage;
+  const int t0 = p - r + 1;
+  const bool ring_needed = t0 < step_start;
+  if (slot >= nslots || t0 < 0 ||
+      (ring_needed && (ring_block < 0 || ring_block >= P.ring_blocks))) {
+    if (threadIdx.x == 0) flag_error(P.err);
+    return;
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int t = t0; t <= p; ++t) {
+    const uint16_t* src =
+        t >= step_start ? P.raw_keys + static_cast<long long>(first_row + (t - step_start)) * kD
+                        : P.ring + (static_cast<long long>(ring_block) * P.S + (t % P.S)) * kD;
+    float x[8];
+    load8_bf16(src + 8 * lane16, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += x[e];
+  }
+  const float inv_r = 1.0f / static_cast<float>(r);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] *= inv_r;
+
+  int64_t pos[3];
+  if (!P.mrope) {
+    pos[0] = pos[1] = pos[2] = t0;
+  } else if (t0 >= step_start) {
+    const long long src_row = first_row + (t0 - step_start);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) pos[k] = P.positions[src_row * 3 + k];
+  } else {
+    const long long ring_slot = static_cast<long long>(ring_block) * P.S + (t0 % P.S);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) pos[k] = P.ring_pos[ring_slot * 3 + k];
+  }
+  float c[8], s[8], w1[8];
+  rope_coeffs(P, lane16, pos, c, s);
+  load8_bf16(P.k_norm_w + 8 * lane16, w1);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) w1[e] += 1.0f;
+  norm_rope(acc, w1, P.eps, lane16, c, s);
+  if (hw == 0) store8<IDT>(P.ccache, slot * kD + 8 * lane16, acc);
+}
+
+// Ring commit: runs after every pooling read of the step.  Each request's
+// newest S raw keys (and 3-D positions) go to their ring slots.  A row writes
+// only if no later row of its request maps to the same slot, which gives the
+// sequential "later rows overwrite earlier rows" result without races.
+__global__ void __launch_bounds__(128) ring_commit_kernel(const CompressParams P) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 4);
+  const int lane16 = threadIdx.x & 15;
+  if (row >= P.rows) return;
+  const int req = P.token_to_req[row];
+  if (req < 0 || req >= P.reqs) return;  // already counted by the compress kernel
+  const int p = P.logical[row];
+  const int p_last = P.logical[P.qsl[req + 1] - 1];
+  if (p + P.S <= p_last) return;  // overwritten later in this step
+  const int ring_block = P.ring_bt[static_cast<long long>(req) * P.ring_bt_stride];
+  if (ring_block < 0 || ring_block >= P.ring_blocks || p < 0) {
+    if (lane16 == 0) flag_error(P.err);
+    return;
+  }
+  const long long ring_slot = static_cast<long long>(ring_block) * P.S + (p % P.S);
+  const uint4 v =
+      *reinterpret_cast<const uint4*>(P.raw_keys + static_cast<long long>(row) * kD + 8 * lane16);
+  *reinterpret_cast<uint4*>(P.ring + ring_slot * kD + 8 * lane16) = v;
+  if (P.ring_pos != nullptr && lane16 < 3) {
+    P.ring_pos[ring_slot * 3 + lane16] = P.positions[static_cast<long long>(row) * 3 + lane16];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const CompressParams& p, cudaStream_t stream) {
+  if (p.rows == 0) return cudaSuccess;
+  if (p.index_dtype == 1)
+    compress_kernel<1><<<p.rows, 128, 0, stream>>>(p);
+  else
+    compress_kernel<0><<<p.rows, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_commit(const CompressParams& p, cudaStream_t stream) {
+  if (p.rows == 0) return cudaSuccess;
+  ring_commit_kernel<<<(p.rows + 7) / 8, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

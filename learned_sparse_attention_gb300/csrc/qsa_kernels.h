@@ -1,0 +1,91 @@
+// Host-side launch interface between the C ABI (abi.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qsa {
+
+struct CompressParams {
+  const uint16_t* projected_q;  // [rows, n_heads*128] bf16 or null
+  void* q_idx;                  // [rows, n_heads, 128] index dtype
+  const uint16_t* raw_keys;     // [rows, 128] bf16
+  const int64_t* positions;     // [rows, 3]
+  const float* cos_sin;         // [max_pos, 64]
+  const uint16_t* q_norm_w;     // [128]
+  const uint16_t* k_norm_w;     // [128]
+  uint16_t* ring;               // [ring_blocks, S, 128]
+  int64_t* ring_pos;            // [ring_blocks, S, 3] or null
+  const int32_t* ring_bt;       // [reqs, ring_bt_stride]
+  const int32_t* token_to_req;
+  const int32_t* qsl;
+  const int32_t* logical;
+  void* ccache;                 // [cpages, cpage, 128] index dtype
+  const int64_t* slots;
+  int ring_blocks, ring_bt_stride, cpages, cpage;
+  int rows, reqs, n_heads, ratio, S, max_pos;
+  int index_dtype, mrope, sec_h, sec_w;
+  float eps;
+  unsigned long long* err;
+};
+
+cudaError_t launch_compress(const CompressParams& p, cudaStream_t stream);
+cudaError_t launch_ring_commit(const CompressParams& p, cudaStream_t stream);
+
+struct LogitsParams {
+  const int32_t* cblock_table;
+  const int32_t* logical;
+  const int32_t* qsl;
+  int4* groups;           // x row0, y nrows, z req
+  int* group_count;
+  float* logits;
+  const uint8_t* ccache;  // read directly by the copy path (cpage not a multiple of 8)
+  long long ld;
+  int cbt_stride, cpages, cpage;
+  int reqs, rows_per_group, max_groups;
+  int n_heads, ratio;
+  float scale;
+  int tiles_per_cta;
+  int manual;
+  int row_bytes;
+  unsigned long long* err;
+};
+
+// Builds the row-group table: each request's rows in chunks of rows_per_group.
+cudaError_t launch_logits_plan(const LogitsParams& p, cudaStream_t stream);
+// npad: padded MMA N (32, 64, 128 or 256); grid = (max_groups, chunks).
+cudaError_t launch_index_logits(const LogitsParams& p, const CUtensorMap& tmap_q,
+                                const CUtensorMap& tmap_k, int index_dtype, int npad,
+                                int max_groups, int chunks, cudaStream_t stream);
+
+struct TopkParams {
+  const float* logits;
+  long long ld;
+  const int32_t* logical;
+  int32_t* packed;
+  int rows, ratio, token_topk, max_visible;
+  unsigned long long* err;
+};
+size_t topk_smem_bytes(int max_visible, int block_topk);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
+
+struct GqaParams {
+  const uint16_t* q;       // [rows, Hq, 128]
+  const uint16_t* kv;      // [blocks, Hkv, page, 256]
+  const int32_t* block_table;
+  const int32_t* packed;
+  const int32_t* token_to_req;
+  const uint16_t* gate;    // nullable
+  uint16_t* out;
+  float* part_o;           // [splits, rows, Hq, 128]
+  float* part_lse;         // [splits, rows, Hq]
+  int bt_stride, packed_width;
+  int rows, hq, hkv, page, num_blocks, splits;
+  unsigned long long* err;
+};
+int gqa_num_splits(int rows, int hkv, int packed_width);
+cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream);
+
+}  // namespace qsa

@@ -1,0 +1,324 @@
+// Stage 4 of the QSA layer step: sparse paged GQA over the selected tokens.
+//
+// Follows "vllm.models.qwen4_exp.nvidia.ops.qsa", qsa_sparse_paged_attention
+// (packed selection buffer whose trailing column is the loop bound, paged
+// K/V through the block table of the row's request, split-KV partials in
+// fp32 merged by log-sum-exp, mandatory output gate) and the patch's
+// _qsa_sparse_paged_gqa_splitk_kernel (score scale D^-1/2 in the exp2
+// domain, invalid entries masked, output divided by the normaliser and zero
+// when nothing is valid, bf16 rounding of the attention output before the
+// sigmoid gate).
+//
+// GB300 mapping.  Decode is an HBM gather: every selected token costs 512
+// contiguous bytes (K then V of one KV head).  One CTA = (row, KV head,
+// split), 4 warps.  Each warp owns 16 tokens of every 64-token tile and runs
+// its own 3-stage cp.async ring over them (16-byte copies, one token row per
+// warp instruction, XOR-swizzled so ldmatrix is conflict-free).  The GQA
+// group of 8 query heads is the N = 8 side of m16n8k16 MMAs with the tokens
+// on M, so no lane is padding:
+//   S^T[16 tok x 8 heads] = K[16 x 128] . Q^T          (8 k-steps)
+//   O^T[128 dims x 8 heads] += V^T[128 x 16] . P^T       (8 m-tiles)
+// P^T comes from the S^T accumulator with one movmatrix transpose per 8x8
+// block; each lane keeps the online-softmax state of its two heads, the same
+// heads its O^T fragments hold.  The four warps are merged in shared memory.
+#include "qsa_device.cuh"
+#include "qsa_kernels.h"
+
+namespace qsa {
+namespace {
+
+constexpr int kG = 8;          // query heads per KV head
+constexpr int kWarps = 4;
+constexpr int kTile = 64;      // tokens per CTA tile (16 per warp)
+constexpr int kStages = 3;
+constexpr int kSlab = 16 * 512;  // bytes per warp stage: 16 tokens x (K|V)
+constexpr int kSmem = kWarps * kStages * kSlab;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
+
+__global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint32_t s_vmask[kWarps][kStages];
+  const int row = blockIdx.x / P.hkv;
+  const int kvh = blockIdx.x % P.hkv;
+  const int split = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int Wcols = P.packed_width - 1;
+
+  const int req = P.token_to_req[row];
+  const int32_t* prow = P.packed + static_cast<long long>(row) * P.packed_width;
+  int n = prow[Wcols];
+  bool bad_row = req < 0;
+  if (n < 0 || n > Wcols) {
+    bad_row = true;
+    n = 0;
+  }
+  if (bad_row) {
+    n = 0;
+    if (threadIdx.x == 0) flag_error(P.err);
+  }
+  const int ntiles = (n + kTile - 1) / kTile;
+  const int tps = (ntiles + P.splits - 1) / P.splits;
+  const int tb = split * tps;
+  const int te = min(ntiles, tb + tps);
+  const int nt = max(0, te - tb);
+
+  // Q^T fragments (B operand of S^T = K.Q^T): head kvh*8 + g, 2 dims per register.
+  const uint16_t* qh = P.q + (static_cast<long long>(row) * P.hq + kvh * kG + g) * 128;
+  uint32_t qb[8][2];
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    qb[kk][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t);
+    qb[kk][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t);
+  }
+
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const float sl2 = 0.08838834764831845f * kLog2e;  // 128^-0.5 * log2(e)
+
+  uint8_t* my = smem + warp * kStages * kSlab;
+  const int32_t* bt_row = P.block_table + static_cast<long long>(req < 0 ? 0 : req) * P.bt_stride;
+
+  auto issue = [&](int tile, int stage) {
+    const int i = tile * kTile + warp * 16 + (lane & 15);
+    long long src_off = 0;
+    int ok = 0;
+    if (lane < 16 && i < n) {
+      const int tok = prow[i];
+      const int blk = tok / P.page;
+      if (tok >= 0 && blk < P.bt_stride) {
+        const int pid = bt_row[blk];
+        if (pid >= 0 && pid < P.num_blocks) {
+          src_off = ((static_cast<long long>(pid) * P.hkv + kvh) * P.page + (tok - blk * P.page)) * 256;
+          ok = 1;
+        }
+      }
+      if (!ok) flag_error(P.err);
+    }
+    const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xffffu;
+    if (lane == 0) s_vmask[warp][stage] = vm;
+    uint8_t* dst_base = my + stage * kSlab;
+    const int chunk = lane & 15, is_v = lane >> 4;
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+      const long long off = __shfl_sync(0xffffffffu, src_off, j);
+      const bool okj = (vm >> j) & 1u;
+      uint8_t* dst = dst_base + is_v * 4096 + j * 256 + ((chunk ^ (j & 7)) << 4);
+      const uint16_t* src = P.kv + off + is_v * 128 + chunk * 8;
+      cp_async16(dst, okj ? static_cast<const void*>(src) : static_cast<const void*>(P.kv),
+                 okj ? 16u : 0u);
+    }
+  };
+
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < nt) issue(tb + s, s);
+    cp_async_commit();
+  }
+  for (int it = 0; it < nt; ++it) {
+    cp_async_wait<kStages - 2>();
+    __syncwarp();
+    const int stage = it % kStages;
+    const uint8_t* sK = my + stage * kSlab;
+    const uint8_t* sV = sK + 4096;
+
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t a[4];
+      const int rl = lane & 15;
+      const int ch = 2 * kk + (lane >> 4);
+      ldmatrix_x4(a, sK + rl * 256 + ((ch ^ (rl & 7)) << 4));
+      mma_bf16_16816(s, a, qb[kk][0], qb[kk][1]);
+    }
+    const uint32_t vm = s_vmask[warp][stage];
+    const bool v0 = (vm >> g) & 1u, v1 = (vm >> (g + 8)) & 1u;
+    const float x0 = v0 ? s[0] * sl2 : -INFINITY;  // token g,   head 2t
+    const float x1 = v0 ? s[1] * sl2 : -INFINITY;  // token g,   head 2t+1
+    const float x2 = v1 ? s[2] * sl2 : -INFINITY;  // token g+8, head 2t
+    const float x3 = v1 ? s[3] * sl2 : -INFINITY;  // token g+8, head 2t+1
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float b0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float b1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(m0 - b0), al1 = exp2f(m1 - b1);
+    const float p0 = exp2f(x0 - b0), p1 = exp2f(x1 - b1);
+    const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
+    l0 = l0 * al0 + p0 + p2;
+    l1 = l1 * al1 + p1 + p3;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] *= al0;
+      o[mt][1] *= al1;
+      o[mt][2] *= al0;
+      o[mt][3] *= al1;
+    }
+    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t a[4];
+      const int tk = (lane & 7) + ((lane >> 4) << 3);
+      const int ch = 2 * mt + ((lane >> 3) & 1);
+      ldmatrix_x4_trans(a, sV + tk * 256 + ((ch ^ (tk & 7)) << 4));
+      mma_bf16_16816(o[mt], a, pb0, pb1);
+    }
+    __syncwarp();
+    const int nxt = it + kStages - 1;
+    if (nxt < nt) issue(tb + nxt, nxt % kStages);
+    cp_async_commit();
+  }
+  cp_async_wait<0>();
+
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  __syncthreads();  // pipeline buffers are free from here on
+  float* cm = reinterpret_cast<float*>(smem);   // [warps][8] max
+  float* cl = cm + kWarps * kG;                 // [warps][8] sum
+  float* co = cl + kWarps * kG;                 // [warps][8 heads][128 dims]
+  if (lane < 4) {
+    cm[warp * kG + 2 * t] = m0;
+    cm[warp * kG + 2 * t + 1] = m1;
+    cl[warp * kG + 2 * t] = l0;
+    cl[warp * kG + 2 * t + 1] = l1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int d = 16 * mt + g;
+    co[(warp * kG + 2 * t) * 128 + d] = o[mt][0];
+    co[(warp * kG + 2 * t + 1) * 128 + d] = o[mt][1];
+    co[(warp * kG + 2 * t) * 128 + d + 8] = o[mt][2];
+    co[(warp * kG + 2 * t + 1) * 128 + d + 8] = o[mt][3];
+  }
+  __syncthreads();
+
+  const int h = threadIdx.x >> 4;          // 0..7
+  const int d0 = (threadIdx.x & 15) * 8;   // 8 dims per thread
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * kG + h]);
+  float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float mw = cm[w * kG + h];
+    const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
+    L += cl[w * kG + h] * wt;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += co[(w * kG + h) * 128 + d0 + e] * wt;
+  }
+  const float inv = L > 0.f ? 1.0f / L : 0.f;
+  const int hq = kvh * kG + h;
+  const long long obase = (static_cast<long long>(row) * P.hq + hq) * 128 + d0;
+  if (P.splits == 1) {
+    float gv[8];
+    if (P.gate != nullptr) {
+      const uint4 gr = *reinterpret_cast<const uint4*>(P.gate + obase);
+      gv[0] = bf16_lo(gr.x); gv[1] = bf16_hi(gr.x); gv[2] = bf16_lo(gr.y); gv[3] = bf16_hi(gr.y);
+      gv[4] = bf16_lo(gr.z); gv[5] = bf16_hi(gr.z); gv[6] = bf16_lo(gr.w); gv[7] = bf16_hi(gr.w);
+    }
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      y[e] = bf16_round(acc[e] * inv);
+      if (P.gate != nullptr) y[e] = y[e] * sigmoidf_(gv[e]);
+    }
+    uint4 ov;
+    ov.x = pack_bf16x2(y[0], y[1]);
+    ov.y = pack_bf16x2(y[2], y[3]);
+    ov.z = pack_bf16x2(y[4], y[5]);
+    ov.w = pack_bf16x2(y[6], y[7]);
+    *reinterpret_cast<uint4*>(P.out + obase) = ov;
+  } else {
+    const long long pbase = (static_cast<long long>(split) * P.rows + row) * P.hq + hq;
+    float4* po = reinterpret_cast<float4*>(P.part_o + pbase * 128 + d0);
+    po[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    po[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+    if ((threadIdx.x & 15) == 0) P.part_lse[pbase] = L > 0.f ? M + __log2f(L) : -INFINITY;
+  }
+}
+
+// Log-sum-exp merge of the split partials, then bf16 rounding and the gate.
+__global__ void __launch_bounds__(256) gqa_merge_kernel(const GqaParams P) {
+  const int row = blockIdx.x;
+  for (int idx = threadIdx.x; idx < P.hq * 16; idx += blockDim.x) {
+    const int hq = idx >> 4, d0 = (idx & 15) * 8;
+    float M = -INFINITY;
+    for (int s = 0; s < P.splits; ++s)
+      M = fmaxf(M, P.part_lse[(static_cast<long long>(s) * P.rows + row) * P.hq + hq]);
+    float W = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < P.splits; ++s) {
+      const long long pb = (static_cast<long long>(s) * P.rows + row) * P.hq + hq;
+      const float lse = P.part_lse[pb];
+      if (lse == -INFINITY) continue;
+      const float wt = exp2f(lse - M);
+      W += wt;
+      const float4* po = reinterpret_cast<const float4*>(P.part_o + pb * 128 + d0);
+      const float4 a = po[0], b = po[1];
+      acc[0] += wt * a.x; acc[1] += wt * a.y; acc[2] += wt * a.z; acc[3] += wt * a.w;
+      acc[4] += wt * b.x; acc[5] += wt * b.y; acc[6] += wt * b.z; acc[7] += wt * b.w;
+    }
+    const float inv = W > 0.f ? 1.0f / W : 0.f;
+    const long long obase = (static_cast<long long>(row) * P.hq + hq) * 128 + d0;
+    float gv[8];
+    if (P.gate != nullptr) {
+      const uint4 gr = *reinterpret_cast<const uint4*>(P.gate + obase);
+      gv[0] = bf16_lo(gr.x); gv[1] = bf16_hi(gr.x); gv[2] = bf16_lo(gr.y); gv[3] = bf16_hi(gr.y);
+      gv[4] = bf16_lo(gr.z); gv[5] = bf16_hi(gr.z); gv[6] = bf16_lo(gr.w); gv[7] = bf16_hi(gr.w);
+    }
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      y[e] = bf16_round(acc[e] * inv);
+      if (P.gate != nullptr) y[e] = y[e] * sigmoidf_(gv[e]);
+    }
+    uint4 ov;
+    ov.x = pack_bf16x2(y[0], y[1]);
+    ov.y = pack_bf16x2(y[2], y[3]);
+    ov.z = pack_bf16x2(y[4], y[5]);
+    ov.w = pack_bf16x2(y[6], y[7]);
+    *reinterpret_cast<uint4*>(P.out + obase) = ov;
+  }
+}
+
+}  // namespace
+
+// Split-KV count: enough CTAs to cover the SMs about twice, never more
+// splits than 64-token tiles.
+int gqa_num_splits(int rows, int hkv, int packed_width) {
+  const long long base = static_cast<long long>(rows) * hkv;
+  if (base <= 0) return 1;
+  const int max_tiles = (packed_width - 1 + kTile - 1) / kTile;
+  const long long target = 2 * 152 * 2;
+  long long s = (target + base - 1) / base;
+  if (s > max_tiles) s = max_tiles;
+  if (s > 32) s = 32;
+  if (s < 1) s = 1;
+  return static_cast<int>(s);
+}
+
+cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream) {
+  if (p.rows == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  gqa_kernel<<<dim3(p.rows * p.hkv, p.splits), 128, kSmem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  gqa_merge_kernel<<<p.rows, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace qsa
