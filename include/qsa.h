@@ -253,6 +253,12 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg,
 size_t qsa_workspace_bytes(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg,
                            int32_t rows, int32_t reqs, int32_t max_visible);
 
+/* Number of kernel launches one qsa_layer_step call makes for these sizes
+ * (compress, ring commit, row-group plan, logits, top-k, sparse GQA and,
+ * with split-KV, its merge; 3 or 4 with skip_topk).  0 if invalid. */
+int32_t qsa_step_launches(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t rows,
+                          int32_t reqs, int32_t skip_topk);
+
 /* Static description of a status code. */
 const char* qsa_status_string(qsa_status status);
 

@@ -455,6 +455,15 @@ size_t qsa_workspace_bytes(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t 
   return L.total;
 }
 
+int32_t qsa_step_launches(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t rows,
+                          int32_t reqs, int32_t skip_topk) {
+  if (check_cfg(cfg) != QSA_OK || check_gcfg(gcfg) != QSA_OK || rows < 0 || reqs < 0) return 0;
+  if (rows == 0) return 0;
+  const int pw = cfg->token_topk + cfg->compress_ratio;
+  const int splits = gqa_num_splits(rows, gcfg->num_kv_heads, pw);
+  return 2 + (skip_topk ? 0 : 3) + 1 + (splits > 1 ? 1 : 0);
+}
+
 const char* qsa_status_string(qsa_status s) {
   switch (s) {
     case QSA_OK: return "ok";

@@ -83,6 +83,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qsa_status_string": [I],
         "qsa_check_errors": [ctypes.POINTER(ctypes.c_int64)],
         "qsa_version": [],
+        "qsa_step_launches": [P, P, I, I, I],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -237,6 +238,12 @@ def layer_step(cfg, gcfg, args: QsaStepArgs, ws, skip_topk=False, stream=None):
                                1 if skip_topk else 0, _ptr(ws, torch.uint8), ws.numel(),
                                _stream(stream))
     _check("qsa_layer_step", st)
+
+
+def step_launches(cfg, gcfg, rows, reqs, skip_topk=False) -> int:
+    """Kernel launches made by one layer_step call."""
+    return int(load().qsa_step_launches(ctypes.byref(cfg), ctypes.byref(gcfg), rows, reqs,
+                                        1 if skip_topk else 0))
 
 
 def check_errors() -> int:

@@ -155,7 +155,7 @@ def _randn(gen, shape, device, dtype=torch.bfloat16, std=1.0):
     return x.to(dtype)
 
 
-def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0) -> Workload:
+def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0, with_caches: bool = True) -> Workload:
     """Build every input of one layer step.  Metadata and small tensors come
     from a CPU generator seeded by (seed, step); the large caches from a
     generator on ``device`` seeded by seed (so they do not depend on step).
@@ -252,6 +252,9 @@ def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0) -> Workload:
         t["ring_pos"] = torch.from_numpy(ring_pos)
 
     dev = torch.device(device)
+    if not with_caches:
+        t = {k: v.to(dev) for k, v in t.items() if k != "ring"}
+        return Workload(spec, t, image_start)
     gd = torch.Generator(device=dev).manual_seed(spec.seed * 1000 + 7)
     t["kv"] = _randn(gd, (n_kv_blocks, spec.hkv, spec.page, 2 * D), dev)
     cc = torch.randn((n_cpages, spec.cpage, 1, D), generator=gd, device=dev, dtype=torch.float32)
@@ -290,6 +293,6 @@ def small_spec(name="small", seed=5, contexts=(37, 64, 301, 5), rows_per_req=(1,
                **kw) -> WorkloadSpec:
     """A small mixed case: several requests, ragged lengths, multi-row steps."""
     base = dict(n_heads=8, index_dtype=DTYPE_BF16, compress_ratio=4, token_topk=64,
-                hq=8, hkv=2, page=16)
+                hq=16, hkv=2, page=16)
     base.update(kw)
     return WorkloadSpec(name, seed, list(contexts), list(rows_per_req), **base)

@@ -1,0 +1,346 @@
+"""CUDA path vs oracle on the same seeded inputs (GB300).
+
+Stage-isolated tests feed each kernel inputs from the seeded generators or
+from the oracle, never from another kernel; the full-chain tests run the
+fused layer step and compare every stage's result with the oracle's own
+chain under the parity rules of tests/parity.py."""
+
+import numpy as np
+import pytest
+import torch
+
+from learned_sparse_attention_gb300 import qsa as Q
+from learned_sparse_attention_gb300 import workloads as W
+from oracle import qsa_oracle as O
+from tests.gpu_harness import (Step, cfgs, idx_dtype, max_visible, oracle_gqa_row, random_packed)
+from tests.oracle_io import OracleState, f64, i64
+from tests.parity import close_bf16, close_e4m3, selection_ok
+
+pytestmark = pytest.mark.gpu
+
+E4, BF = W.DTYPE_E4M3, W.DTYPE_BF16
+
+MID = {
+    "tiny_bf16": W.named_spec("tiny_bf16"),
+    "small_bf16_copy_path": W.small_spec("small_bf16_copy_path", seed=5),
+    "small_e4m3_copy_path": W.small_spec("small_e4m3_copy_path", seed=6, index_dtype=E4),
+    "mid_e4m3_r4": W.small_spec("mid_e4m3_r4", seed=11, contexts=(1999, 4096, 777, 63, 5, 2500),
+                                rows_per_req=(1, 3, 2, 1, 1, 8), n_heads=32, index_dtype=E4,
+                                compress_ratio=4, token_topk=256, hq=32, hkv=4, page=64),
+    "mid_bf16_r8_h16": W.small_spec("mid_bf16_r8_h16", seed=12, contexts=(3001, 1024, 40, 9000),
+                                    rows_per_req=(2, 1, 1, 4), n_heads=16, index_dtype=BF,
+                                    compress_ratio=8, token_topk=512, hq=16, hkv=2, page=64),
+    "mid_mrope_h8": W.small_spec("mid_mrope_h8", seed=13, contexts=(3000, 2048, 700),
+                                 rows_per_req=(4, 4, 4), n_heads=8, index_dtype=BF,
+                                 compress_ratio=4, token_topk=128, mrope_section=(8, 12, 12),
+                                 image_span=64, hq=32, hkv=4, page=32),
+    "mid_h64_e4m3_r2": W.small_spec("mid_h64_e4m3_r2", seed=14, contexts=(5000, 300),
+                                    rows_per_req=(2, 1), n_heads=64, index_dtype=E4,
+                                    compress_ratio=2, token_topk=256, hq=64, hkv=8, page=16),
+}
+
+
+def _close_idx(spec, got, want):
+    return close_e4m3(got, want) if spec.index_dtype == E4 else close_bf16(got, want)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    Q.load()
+    Q.check_errors()
+    yield
+    assert Q.check_errors() == 0
+
+
+# ----------------------------------------------------------------- stage 1
+@pytest.mark.parametrize("name", list(MID))
+def test_compress_matches_oracle(name):
+    spec = MID[name]
+    wl = W.make_workload(spec, device="cuda")
+    st = OracleState(wl, with_kv=False)
+    cc_before = st.ccache.copy()
+    cfg, _ = cfgs(spec, wl)
+    q_idx = torch.zeros((spec.rows, spec.n_heads, 128), dtype=idx_dtype(spec), device="cuda")
+    t = wl.t
+    Q.compress(cfg, t["projected_q"], q_idx, t["raw_keys"], t["positions"], t["cos_sin"],
+               t["q_norm_w"], t["k_norm_w"], t["ring"], t.get("ring_pos"), t["ring_block_table"],
+               t["token_to_req"], t["query_start_loc"], t["logical_positions"], t["ccache"],
+               t["compressed_slots"])
+    torch.cuda.synchronize()
+    oq, written = st.compress()
+    ok, err = _close_idx(spec, f64(q_idx), oq)
+    assert ok, f"q_idx {err}"
+    got_cc = f64(t["ccache"]).reshape(st.ccache.shape)
+    slots = [s for _, s, _ in written]
+    assert len(slots) == int((i64(t["compressed_slots"]) >= 0).sum())
+    flat_got = got_cc.reshape(-1, 128)
+    flat_want = st.ccache.reshape(-1, 128)
+    ok, err = _close_idx(spec, flat_got[slots], flat_want[slots])
+    assert ok, f"compressed keys {err}"
+    untouched = np.setdiff1d(np.arange(flat_got.shape[0]), slots)
+    np.testing.assert_array_equal(flat_got[untouched], cc_before.reshape(-1, 128)[untouched])
+    np.testing.assert_array_equal(f64(t["ring"]).reshape(st.ring.shape), st.ring)
+    if st.ring_pos is not None:
+        np.testing.assert_array_equal(i64(t["ring_pos"]).reshape(st.ring_pos.shape), st.ring_pos)
+
+
+# ----------------------------------------------------------------- stage 2
+@pytest.mark.parametrize("name", list(MID))
+def test_index_logits_matches_oracle(name):
+    spec = MID[name]
+    wl = W.make_workload(spec, device="cuda")
+    cfg, _ = cfgs(spec, wl)
+    st = OracleState(wl, with_kv=False)
+    g = torch.Generator(device="cuda").manual_seed(77)
+    qf = torch.randn((spec.rows, spec.n_heads, 128), generator=g, device="cuda")
+    q_idx = (qf.to(torch.float8_e4m3fn).view(torch.uint8) if spec.index_dtype == E4
+             else qf.to(torch.bfloat16))
+    mv = max_visible(spec)
+    ld = (mv + 3) // 4 * 4
+    logits = torch.full((spec.rows, ld), float("nan"), device="cuda")
+    ws = torch.empty(Q.workspace_bytes(cfg, cfgs(spec, wl)[1], spec.rows, spec.reqs, mv),
+                     dtype=torch.uint8, device="cuda")
+    t = wl.t
+    Q.index_logits(cfg, q_idx, t["ccache"], t["cblock_table"], t["token_to_req"],
+                   t["query_start_loc"], t["logical_positions"], logits, mv, ws)
+    torch.cuda.synchronize()
+    got = logits.cpu().numpy().astype(np.float64)
+    qv = f64(q_idx)
+    worst = 0.0
+    for row in range(spec.rows):
+        p = int(st.logical_positions[row])
+        V = O.visible_blocks(p, spec.compress_ratio)
+        if V == 0:
+            continue
+        req = int(st.token_to_req[row])
+        keys = O.gather_compressed_keys(st.cfg, st.ccache, st.cblock_table[req], V)
+        want = O.index_logits_row(st.cfg, qv[row], keys)
+        # fp32 accumulation of exact products: relative error ~1e-6 of the
+        # sum of |terms|; bound it by 1e-4 of the row's score scale.
+        tol = 1e-4 * ((np.abs(keys) @ np.abs(qv[row]).T).sum(1) / (spec.n_heads * np.sqrt(128))
+                      + 1e-3)
+        e = np.abs(got[row, :V] - want)
+        worst = max(worst, float((e / tol).max()))
+        assert (e <= tol).all(), f"row {row}: max err {e.max():.3g}"
+    print(f"{name}: worst logits error / tolerance = {worst:.3g}")
+
+
+# ----------------------------------------------------------------- stage 3
+@pytest.mark.parametrize("ratio,topk,positions", [
+    (4, 64, [0, 2, 3, 62, 63, 64, 255, 299, 1000, 4095]),
+    (4, 2048, [8191, 20000, 32767, 2046, 2047, 8000]),
+    (8, 4096, [131071, 65535, 32767, 1000]),
+    (2, 256, [1, 5, 511, 512, 999]),
+])
+@pytest.mark.parametrize("ties", [False, True])
+def test_topk_matches_oracle(ratio, topk, positions, ties):
+    cfg_o = O.QsaConfig(n_heads=8, compress_ratio=ratio, token_topk=topk)
+    cfg = Q.make_cfg(8, ratio, topk, BF, 16, 10)
+    logical = np.array(positions, dtype=np.int32)
+    mv = int(max((p + 1) // ratio for p in positions))
+    rng = np.random.default_rng(ratio * 1000 + topk + ties)
+    if ties:  # few distinct values: many exact ties at the selection boundary
+        vals = rng.integers(0, 7, size=(len(positions), mv)).astype(np.float32) / 8
+    else:
+        vals = rng.standard_normal((len(positions), mv)).astype(np.float32)
+    logits = torch.from_numpy(vals).cuda()
+    packed = torch.full((len(positions), cfg_o.packed_width), -9, dtype=torch.int32, device="cuda")
+    Q.topk(cfg, logits, mv, torch.from_numpy(logical).cuda(), packed)
+    torch.cuda.synchronize()
+    got = packed.cpu().numpy()
+    for i, p in enumerate(positions):
+        V = O.visible_blocks(p, ratio)
+        blocks = O.select_blocks(vals[i, :V].astype(np.float64), V, cfg_o.block_topk)
+        np.testing.assert_array_equal(got[i], O.expand_row(cfg_o, blocks, p))
+
+
+# ----------------------------------------------------------------- stage 4
+@pytest.mark.parametrize("name", ["tiny_bf16", "small_bf16_copy_path", "mid_e4m3_r4",
+                                  "mid_h64_e4m3_r2", "mid_mrope_h8"])
+@pytest.mark.parametrize("gate", [True, False])
+def test_sparse_gqa_matches_oracle(name, gate):
+    spec = MID[name]
+    wl = W.make_workload(spec, device="cuda")
+    st = OracleState(wl)
+    _, gcfg = cfgs(spec, wl)
+    rng = np.random.default_rng(5)
+    packed_np = random_packed(rng, st.cfg, st.logical_positions, full_rows={0})
+    packed_np[-1, :] = -1
+    packed_np[-1, -1] = 0  # an empty row: output must be zero
+    packed = torch.from_numpy(packed_np).cuda()
+    out = torch.full_like(wl["q"], 3.0)
+    ws = torch.empty(1 << 24, dtype=torch.uint8, device="cuda")
+    Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], packed, wl["token_to_req"],
+                 wl["gate"] if gate else None, out, ws)
+    torch.cuda.synchronize()
+    got = f64(out)
+    for row in range(spec.rows):
+        n = int(packed_np[row, -1])
+        req = int(st.token_to_req[row])
+        want = O.sparse_gqa_row(st.q[row], st.kv, st.block_table[req], packed_np[row, :n],
+                                spec.page, st.gate[row] if gate else None)
+        ok, err = close_bf16(got[row], want)
+        assert ok, f"row {row} (n={n}): max err {err:.3g}"
+    assert (got[-1] == 0).all()
+
+
+def test_split_kv_invariance():
+    """A row computed alone (split-KV over many CTAs + merge) equals the same
+    row inside a large batch (one CTA per row and KV head)."""
+    spec = W.small_spec("split", seed=21, contexts=[3000] * 80, rows_per_req=[1] * 80,
+                        n_heads=8, index_dtype=BF, compress_ratio=4, token_topk=512,
+                        hq=32, hkv=4, page=64)
+    wl = W.make_workload(spec, device="cuda")
+    _, gcfg = cfgs(spec, wl)
+    st = OracleState(wl, with_kv=False)
+    rng = np.random.default_rng(8)
+    packed = torch.from_numpy(random_packed(rng, st.cfg, st.logical_positions,
+                                            full_rows=set(range(80)))).cuda()
+    ws = torch.empty(1 << 26, dtype=torch.uint8, device="cuda")
+    out_all = torch.empty_like(wl["q"])
+    Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], packed, wl["token_to_req"],
+                 wl["gate"], out_all, ws)
+    for row in (0, 37, 79):
+        one = torch.empty_like(wl["q"][row:row + 1])
+        Q.sparse_gqa(gcfg, wl["q"][row:row + 1].contiguous(), wl["kv"], wl["block_table"],
+                     packed[row:row + 1].contiguous(), wl["token_to_req"][row:row + 1].contiguous(),
+                     wl["gate"][row:row + 1].contiguous(), one, ws)
+        torch.cuda.synchronize()
+        ok, err = close_bf16(f64(one[0]), f64(out_all[row]))
+        assert ok, err
+
+
+# ----------------------------------------------------------------- full chain
+def _full_chain(spec, wl, st, step, rows=None, packed_ref=None, skip=False):
+    """Compare a finished GPU step with the oracle's own chain on `rows`."""
+    rows = range(spec.rows) if rows is None else rows
+    got_packed = step.packed.cpu().numpy()
+    got_out = f64(step.out)
+    tie_rows = 0
+    for row in rows:
+        p = int(st.logical_positions[row])
+        req = int(st.token_to_req[row])
+        if skip:
+            opack = packed_ref[row]
+            np.testing.assert_array_equal(got_packed[row], opack)
+        else:
+            qrow = O.prep_query(st.cfg, st.projected_q[row], st.positions[row], st.cos_sin,
+                                st.q_norm_w)
+            scores, _, opack = O.select_row(st.cfg, qrow, st.ccache, st.cblock_table[req], p)
+            ok, ndiff = selection_ok(st.cfg, got_packed[row], opack, scores, p)
+            assert ok, f"{spec.name} row {row}: selection differs beyond the tie window"
+            if ndiff:
+                tie_rows += 1
+                continue
+        n = int(opack[-1])
+        if st.kv is not None:
+            want = O.sparse_gqa_row(st.q[row], st.kv, st.block_table[req], opack[:n], spec.page,
+                                    st.gate[row])
+        else:
+            want = oracle_gqa_row(st.q[row], step.wl["kv"], st.block_table[req], opack[:n],
+                                  spec.page, st.gate[row])
+        ok, err = close_bf16(got_out[row], want)
+        assert ok, f"{spec.name} row {row}: output err {err:.3g}"
+    return tie_rows
+
+
+@pytest.mark.parametrize("name", list(MID))
+def test_layer_step_full_chain(name):
+    spec = MID[name]
+    wl = W.make_workload(spec, device="cuda")
+    st = OracleState(wl)
+    step = Step(wl).run()
+    st.compress()  # the oracle's stage 1 (caches now hold this step's groups)
+    ties = _full_chain(spec, wl, st, step)
+    assert ties <= max(1, spec.rows // 10)
+    np.testing.assert_array_equal(f64(wl["ring"]).reshape(st.ring.shape), st.ring)
+
+
+def test_skip_topk_reuses_selection_and_updates_caches():
+    spec = MID["mid_mrope_h8"]
+    wl = W.make_workload(spec, device="cuda")
+    step = Step(wl).run()
+    packed0 = step.packed.cpu().numpy().copy()
+    st = OracleState(wl)  # caches after step 0
+    nxt = W.make_workload(spec, device="cuda", step=1, with_caches=False)
+    for k in ("projected_q", "raw_keys", "q", "gate"):
+        wl.t[k].copy_(nxt[k])
+        setattr(st, k, f64(nxt[k]).reshape(getattr(st, k).shape))
+    step.packed.copy_(torch.from_numpy(packed0))
+    step.run(skip_topk=True)
+    st.compress()
+    _full_chain(spec, wl, st, step, packed_ref=packed0, skip=True)
+    np.testing.assert_array_equal(f64(wl["ring"]).reshape(st.ring.shape), st.ring)
+
+
+def test_empty_batch_is_noop():
+    spec = MID["tiny_bf16"]
+    wl = W.make_workload(spec, device="cuda")
+    cfg, gcfg = cfgs(spec, wl)
+    a = Q.QsaStepArgs()
+    a.rows, a.reqs = 0, 0
+    a.packed = wl["q"].data_ptr()
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    Q.layer_step(cfg, gcfg, a, ws)
+
+
+def test_out_of_range_pages_are_masked_and_counted():
+    spec = MID["tiny_bf16"]
+    wl = W.make_workload(spec, device="cuda")
+    Q.check_errors()
+    wl.t["block_table"][0, 0] = 10 ** 6  # no such KV block
+    Step(wl).run()
+    assert Q.check_errors() > 0
+    assert Q.check_errors() == 0  # the word is cleared by the read
+
+
+# ----------------------------------------------------------------- full size
+def _sampled(name, nsample, seed=0):
+    spec = W.named_spec(name)
+    wl = W.make_workload(spec, device="cuda")
+    st = OracleState(wl, with_kv=False)
+    step = Step(wl).run()
+    assert Q.check_errors() == 0
+    # oracle stage 1 keys for every row (query prep only for sampled rows)
+    O.compress_stage(st.cfg, projected_q=None, raw_keys=st.raw_keys, positions=st.positions,
+                     cos_sin=st.cos_sin, q_norm_w=st.q_norm_w, k_norm_w=st.k_norm_w,
+                     ring=st.ring, ring_pos=st.ring_pos, ring_block_table=st.ring_block_table,
+                     token_to_req=st.token_to_req, query_start_loc=st.query_start_loc,
+                     logical_positions=st.logical_positions, ccache=st.ccache,
+                     compressed_slots=st.compressed_slots)
+    rng = np.random.default_rng(seed)
+    rows = np.arange(spec.rows) if spec.rows <= nsample else np.sort(
+        rng.choice(spec.rows, size=nsample, replace=False))
+    ties = _full_chain(spec, wl, st, step, rows=rows)
+    # compressed keys written by the step
+    slots = i64(wl["compressed_slots"])
+    sl = slots[slots >= 0]
+    got = f64(wl["ccache"]).reshape(-1, 128)[sl]
+    ok, err = _close_idx(spec, got, st.ccache.reshape(-1, 128)[sl])
+    assert ok, err
+    return spec, step, ties, len(rows)
+
+
+@pytest.mark.parametrize("name,nsample", [("decode_batch", 64), ("long_decode", 8),
+                                          ("mtp_mrope", 128), ("chunked_prefill", 192)])
+def test_full_size_sampled_rows(name, nsample):
+    spec, step, ties, n = _sampled(name, nsample)
+    assert ties <= max(2, n // 10), f"{ties} tie rows out of {n}"
+    print(f"{name}: {n} rows checked, {ties} rows differ only inside the tie window")
+
+
+def test_full_size_invariants_decode_batch():
+    """Properties that hold for every row at full size: counts, causality,
+    uniqueness, -1 padding."""
+    spec = W.named_spec("decode_batch")
+    wl = W.make_workload(spec, device="cuda")
+    step = Step(wl).run()
+    pk = step.packed.cpu().numpy()
+    cfg = O.QsaConfig(n_heads=32, compress_ratio=4, token_topk=2048)
+    for row, p in enumerate(i64(wl["logical_positions"])):
+        n = pk[row, -1]
+        assert n == O.expected_count(cfg, int(p))
+        toks = pk[row, :n]
+        assert toks.min() >= 0 and toks.max() <= p and len(np.unique(toks)) == n
+        assert (pk[row, n:-1] == -1).all()
+    assert np.isfinite(f64(step.out)).all()
