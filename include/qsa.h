@@ -201,6 +201,33 @@ qsa_status qsa_sparse_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv
                           void* out, int32_t rows, void* ws, size_t ws_bytes,
                           void* stream);
 
+/*
+ * qsa_sparse_gqa_noalloc -- qsa_sparse_gqa for callers that cannot allocate.
+ * No counterpart on the pages the method comes from: this is a library
+ * convenience.  Some callers may not allocate device memory where attention
+ * runs (an allocator frozen after start-up, a memory pool owned by someone
+ * else, a plugin host that hands over only the call's tensors), so they
+ * cannot provide the workspace qsa_sparse_gqa wants.  This variant keeps its
+ * split-KV scratch in a static device array inside the library:
+ * QSA_NOALLOC_SCRATCH_BYTES on every GPU that loads the library, held until
+ * the process exits.  Arguments and results are those of qsa_sparse_gqa
+ * without ws / ws_bytes; it allocates nothing.
+ *  - Sizes whose split-KV partials need more than QSA_NOALLOC_SCRATCH_BYTES
+ *    are rejected with QSA_ERR_WORKSPACE before anything is launched.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents (nothing in it has to start at zero).  Calls that can overlap
+ *    on the GPU race on it: order them on one stream or with events.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current and caches it; make that first call before any
+ *    stream capture.
+ */
+#define QSA_NOALLOC_SCRATCH_BYTES (4u << 20)
+qsa_status qsa_sparse_gqa_noalloc(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
+                                  const int32_t* block_table, int32_t bt_stride,
+                                  const int32_t* packed, int32_t packed_width,
+                                  const int32_t* token_to_req, const void* gate, void* out,
+                                  int32_t rows, void* stream);
+
 /* Arguments of one fused layer step (all device pointers; meanings as in the
  * stage calls above). */
 typedef struct qsa_step_args {

@@ -364,6 +364,10 @@ bool step_layout(const qsa_cfg* c, const qsa_gqa_cfg* g, int rows, int reqs, int
 }
 
 }  // namespace
+
+// Error word of the current device, for entry points defined in other files.
+unsigned long long* internal_error_word() { return error_word(); }
+
 }  // namespace qsa
 
 using namespace qsa;

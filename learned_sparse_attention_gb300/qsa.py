@@ -192,6 +192,24 @@ def sparse_gqa(gcfg, q, kv, block_table, packed, token_to_req, gate, out, ws, st
     _check("qsa_sparse_gqa", st)
 
 
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def sparse_gqa_noalloc(gcfg, q, kv, block_table, packed, token_to_req, gate, out, stream=None):
+    """Stage 4 without a workspace: for callers that may not allocate device
+    memory; the split-KV scratch is a fixed array inside the library (see
+    qsa_sparse_gqa_noalloc in include/qsa.h for its limit and sharing rules)."""
+    lib = load()
+    f = lib.qsa_sparse_gqa_noalloc
+    f.argtypes = [_p, _p, _p, _p, _c_int, _p, _c_int, _p, _p, _p, _c_int, _p]
+    f.restype = ctypes.c_int
+    st = f(ctypes.byref(gcfg), _ptr(q, torch.bfloat16), _ptr(kv, torch.bfloat16),
+           _ptr(block_table, torch.int32), block_table.shape[1], _ptr(packed, torch.int32),
+           packed.shape[1], _ptr(token_to_req, torch.int32), _ptr(gate, torch.bfloat16),
+           _ptr(out, torch.bfloat16), q.shape[0], _stream(stream))
+    _check("qsa_sparse_gqa_noalloc", st)
+
+
 def workspace_bytes(cfg, gcfg, rows, reqs, max_visible) -> int:
     return int(load().qsa_workspace_bytes(ctypes.byref(cfg), ctypes.byref(gcfg), rows, reqs,
                                           max_visible))
