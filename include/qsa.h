@@ -281,10 +281,14 @@ size_t qsa_workspace_bytes(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg,
                            int32_t rows, int32_t reqs, int32_t max_visible);
 
 /* Number of kernel launches one qsa_layer_step call makes for these sizes
- * (compress, ring commit, row-group plan, logits, top-k, sparse GQA and,
- * with split-KV, its merge; 3 or 4 with skip_topk).  0 if invalid. */
+ * (compress, ring commit, row-group plan, logits, top-k and sparse GQA; 3
+ * with skip_topk).  0 if invalid. */
 int32_t qsa_step_launches(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t rows,
                           int32_t reqs, int32_t skip_topk);
+
+/* Split-KV factor qsa_sparse_gqa uses for `rows` rows (1 = no split, no
+ * scratch).  0 if invalid. */
+int32_t qsa_gqa_splits(const qsa_gqa_cfg* gcfg, int32_t rows, int32_t packed_width);
 
 /* Static description of a status code. */
 const char* qsa_status_string(qsa_status status);

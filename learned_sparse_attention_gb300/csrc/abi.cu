@@ -133,7 +133,8 @@ size_t gqa_ws_bytes(const qsa_gqa_cfg* g, int rows, int packed_width) {
   if (s == 1) return 0;
   const size_t po = static_cast<size_t>(s) * rows * g->num_q_heads * 128 * sizeof(float);
   const size_t pl = static_cast<size_t>(s) * rows * g->num_q_heads * sizeof(float);
-  return align256(po) + align256(pl);
+  const size_t tickets = static_cast<size_t>(rows) * g->num_kv_heads * sizeof(unsigned);
+  return align256(po) + align256(pl) + align256(tickets);
 }
 
 qsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA; }
@@ -330,8 +331,10 @@ qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255)) return QSA_ERR_WORKSPACE;
     if (ws_bytes < gqa_ws_bytes(gcfg, rows, packed_width)) return QSA_ERR_WORKSPACE;
     const size_t po = static_cast<size_t>(p.splits) * rows * p.hq * 128 * sizeof(float);
+    const size_t pl = static_cast<size_t>(p.splits) * rows * p.hq * sizeof(float);
     p.part_o = static_cast<float*>(ws);
     p.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(po));
+    p.counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + align256(po) + align256(pl));
   }
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
@@ -465,7 +468,13 @@ int32_t qsa_step_launches(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t r
   if (rows == 0) return 0;
   const int pw = cfg->token_topk + cfg->compress_ratio;
   const int splits = gqa_num_splits(rows, gcfg->num_kv_heads, pw);
-  return 2 + (skip_topk ? 0 : 3) + 1 + (splits > 1 ? 1 : 0);
+  (void)splits;  // split-KV partials are merged inside the GQA kernel
+  return 2 + (skip_topk ? 0 : 3) + 1;
+}
+
+int32_t qsa_gqa_splits(const qsa_gqa_cfg* gcfg, int32_t rows, int32_t packed_width) {
+  if (check_gcfg(gcfg) != QSA_OK || rows <= 0 || packed_width < 2) return 0;
+  return gqa_num_splits(rows, gcfg->num_kv_heads, packed_width);
 }
 
 const char* qsa_status_string(qsa_status s) {

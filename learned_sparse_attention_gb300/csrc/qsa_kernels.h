@@ -81,6 +81,7 @@ struct GqaParams {
   uint16_t* out;
   float* part_o;           // [splits, rows, Hq, 128]
   float* part_lse;         // [splits, rows, Hq]
+  unsigned* counters;      // [rows, Hkv] merge tickets, or null for a separate merge launch
   int bt_stride, packed_width;
   int rows, hq, hkv, page, num_blocks, splits;
   unsigned long long* err;

@@ -21,6 +21,12 @@
 // P^T comes from the S^T accumulator with one movmatrix transpose per 8x8
 // block; each lane keeps the online-softmax state of its two heads, the same
 // heads its O^T fragments hold.  The four warps are merged in shared memory.
+// A prologue resolves the CTA's whole token range (packed index -> block
+// table -> KV row id) into shared memory in parallel, so the copy issue of a
+// slab never waits on a dependent global load.  With split-KV, the last CTA
+// of a (row, KV head) to finish merges the fp32 partials (an atomic ticket
+// per (row, KV head)), so no second launch is needed when a ticket array is
+// given.
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
 
@@ -32,14 +38,67 @@ constexpr int kWarps = 4;
 constexpr int kTile = 64;      // tokens per CTA tile (16 per warp)
 constexpr int kStages = 3;
 constexpr int kSlab = 16 * 512;  // bytes per warp stage: 16 tokens x (K|V)
-constexpr int kSmem = kWarps * kStages * kSlab;
+constexpr int kPipe = kWarps * kStages * kSlab;
+constexpr int kMaxTiles = 40;                // tiles of one CTA
+constexpr int kMaxTok = kMaxTiles * kTile;   // token row ids staged per CTA
+constexpr int kSmem = kPipe + kMaxTok * 4;
+constexpr uint32_t kBadRow = 0xFFFFFFFFu;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
 
+__device__ __forceinline__ void load_gate8(const uint16_t* gate, long long obase, float (&gv)[8]) {
+  const uint4 gr = *reinterpret_cast<const uint4*>(gate + obase);
+  gv[0] = bf16_lo(gr.x); gv[1] = bf16_hi(gr.x); gv[2] = bf16_lo(gr.y); gv[3] = bf16_hi(gr.y);
+  gv[4] = bf16_lo(gr.z); gv[5] = bf16_hi(gr.z); gv[6] = bf16_lo(gr.w); gv[7] = bf16_hi(gr.w);
+}
+
+// out[8 dims] = bf16(bf16(x) * sigmoid(gate)) (or bf16(x) without a gate).
+__device__ __forceinline__ void store_out8(const GqaParams& P, long long obase, const float (&x)[8]) {
+  float gv[8];
+  if (P.gate != nullptr) load_gate8(P.gate, obase, gv);
+  float y[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    y[e] = bf16_round(x[e]);
+    if (P.gate != nullptr) y[e] = y[e] * sigmoidf_(gv[e]);
+  }
+  uint4 ov;
+  ov.x = pack_bf16x2(y[0], y[1]);
+  ov.y = pack_bf16x2(y[2], y[3]);
+  ov.z = pack_bf16x2(y[4], y[5]);
+  ov.w = pack_bf16x2(y[6], y[7]);
+  *reinterpret_cast<uint4*>(P.out + obase) = ov;
+}
+
+// Log-sum-exp merge of the split partials of 8 dims of one (row, head).
+__device__ __forceinline__ void merge8(const GqaParams& P, int row, int hq, int d0) {
+  float M = -INFINITY;
+  for (int s = 0; s < P.splits; ++s)
+    M = fmaxf(M, __ldcg(P.part_lse + (static_cast<long long>(s) * P.rows + row) * P.hq + hq));
+  float W = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < P.splits; ++s) {
+    const long long pb = (static_cast<long long>(s) * P.rows + row) * P.hq + hq;
+    const float lse = __ldcg(P.part_lse + pb);
+    if (lse == -INFINITY) continue;
+    const float wt = exp2f(lse - M);
+    W += wt;
+    const float4* po = reinterpret_cast<const float4*>(P.part_o + pb * 128 + d0);
+    const float4 a = __ldcg(po), b = __ldcg(po + 1);
+    acc[0] += wt * a.x; acc[1] += wt * a.y; acc[2] += wt * a.z; acc[3] += wt * a.w;
+    acc[4] += wt * b.x; acc[5] += wt * b.y; acc[6] += wt * b.z; acc[7] += wt * b.w;
+  }
+  const float inv = W > 0.f ? 1.0f / W : 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] *= inv;
+  store_out8(P, (static_cast<long long>(row) * P.hq + hq) * 128 + d0, acc);
+}
+
 __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_vmask[kWarps][kStages];
+  __shared__ int s_last;
+  uint32_t* s_rowid = reinterpret_cast<uint32_t*>(smem + kPipe);
   const int row = blockIdx.x / P.hkv;
   const int kvh = blockIdx.x % P.hkv;
   const int split = blockIdx.y;
@@ -64,6 +123,12 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
   const int tb = split * tps;
   const int te = min(ntiles, tb + tps);
   const int nt = max(0, te - tb);
+  const int tok0 = tb * kTile;
+  int ntok = nt > 0 ? min(te * kTile, n) - tok0 : 0;
+  if (ntok > kMaxTok) {  // excluded by gqa_num_splits; never read past the stage
+    if (threadIdx.x == 0) flag_error(P.err);
+    ntok = kMaxTok;
+  }
 
   // Q^T fragments (B operand of S^T = K.Q^T): head kvh*8 + g, 2 dims per register.
   const uint16_t* qh = P.q + (static_cast<long long>(row) * P.hq + kvh * kG + g) * 128;
@@ -83,34 +148,37 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
   uint8_t* my = smem + warp * kStages * kSlab;
   const int32_t* bt_row = P.block_table + static_cast<long long>(req < 0 ? 0 : req) * P.bt_stride;
 
-  auto issue = [&](int tile, int stage) {
-    const int i = tile * kTile + warp * 16 + (lane & 15);
-    long long src_off = 0;
-    int ok = 0;
-    if (lane < 16 && i < n) {
-      const int tok = prow[i];
-      const int blk = tok / P.page;
-      if (tok >= 0 && blk < P.bt_stride) {
-        const int pid = bt_row[blk];
-        if (pid >= 0 && pid < P.num_blocks) {
-          src_off = ((static_cast<long long>(pid) * P.hkv + kvh) * P.page + (tok - blk * P.page)) * 256;
-          ok = 1;
-        }
-      }
-      if (!ok) flag_error(P.err);
+  // Prologue: KV row id (block * Hkv + kvh) * page + offset of every token of
+  // this CTA's range, or kBadRow for a masked entry.
+  for (int i = threadIdx.x; i < ntok; i += blockDim.x) {
+    const int tok = prow[tok0 + i];
+    uint32_t rid = kBadRow;
+    const int blk = tok >= 0 ? tok / P.page : -1;
+    if (tok >= 0 && blk < P.bt_stride) {
+      const int pid = bt_row[blk];
+      if (pid >= 0 && pid < P.num_blocks)
+        rid = static_cast<uint32_t>((static_cast<long long>(pid) * P.hkv + kvh) * P.page +
+                                    (tok - blk * P.page));
     }
-    const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xffffu;
+    if (rid == kBadRow) flag_error(P.err);
+    s_rowid[i] = rid;
+  }
+  __syncthreads();
+
+  auto issue = [&](int tile, int stage) {
+    const int li = tile * kTile + warp * 16 + (lane & 15) - tok0;
+    const uint32_t rid = (lane < 16 && li < ntok) ? s_rowid[li] : kBadRow;
+    const uint32_t vm = __ballot_sync(0xffffffffu, rid != kBadRow) & 0xffffu;
     if (lane == 0) s_vmask[warp][stage] = vm;
     uint8_t* dst_base = my + stage * kSlab;
     const int chunk = lane & 15, is_v = lane >> 4;
 #pragma unroll 4
     for (int j = 0; j < 16; ++j) {
-      const long long off = __shfl_sync(0xffffffffu, src_off, j);
+      const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
       const bool okj = (vm >> j) & 1u;
       uint8_t* dst = dst_base + is_v * 4096 + j * 256 + ((chunk ^ (j & 7)) << 4);
-      const uint16_t* src = P.kv + off + is_v * 128 + chunk * 8;
-      cp_async16(dst, okj ? static_cast<const void*>(src) : static_cast<const void*>(P.kv),
-                 okj ? 16u : 0u);
+      const uint16_t* src = P.kv + static_cast<long long>(okj ? rj : 0u) * 256 + is_v * 128 + chunk * 8;
+      cp_async16(dst, src, okj ? 16u : 0u);
     }
   };
 
@@ -222,101 +290,74 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
   }
   const float inv = L > 0.f ? 1.0f / L : 0.f;
   const int hq = kvh * kG + h;
-  const long long obase = (static_cast<long long>(row) * P.hq + hq) * 128 + d0;
-  if (P.splits == 1) {
-    float gv[8];
-    if (P.gate != nullptr) {
-      const uint4 gr = *reinterpret_cast<const uint4*>(P.gate + obase);
-      gv[0] = bf16_lo(gr.x); gv[1] = bf16_hi(gr.x); gv[2] = bf16_lo(gr.y); gv[3] = bf16_hi(gr.y);
-      gv[4] = bf16_lo(gr.z); gv[5] = bf16_hi(gr.z); gv[6] = bf16_lo(gr.w); gv[7] = bf16_hi(gr.w);
-    }
-    float y[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      y[e] = bf16_round(acc[e] * inv);
-      if (P.gate != nullptr) y[e] = y[e] * sigmoidf_(gv[e]);
-    }
-    uint4 ov;
-    ov.x = pack_bf16x2(y[0], y[1]);
-    ov.y = pack_bf16x2(y[2], y[3]);
-    ov.z = pack_bf16x2(y[4], y[5]);
-    ov.w = pack_bf16x2(y[6], y[7]);
-    *reinterpret_cast<uint4*>(P.out + obase) = ov;
-  } else {
-    const long long pbase = (static_cast<long long>(split) * P.rows + row) * P.hq + hq;
-    float4* po = reinterpret_cast<float4*>(P.part_o + pbase * 128 + d0);
-    po[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-    po[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-    if ((threadIdx.x & 15) == 0) P.part_lse[pbase] = L > 0.f ? M + __log2f(L) : -INFINITY;
+  for (int e = 0; e < 8; ++e) acc[e] *= inv;
+  if (P.splits == 1) {
+    store_out8(P, (static_cast<long long>(row) * P.hq + hq) * 128 + d0, acc);
+    return;
   }
+  const long long pbase = (static_cast<long long>(split) * P.rows + row) * P.hq + hq;
+  float4* po = reinterpret_cast<float4*>(P.part_o + pbase * 128 + d0);
+  po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  if ((threadIdx.x & 15) == 0) P.part_lse[pbase] = L > 0.f ? M + __log2f(L) : -INFINITY;
+  if (P.counters == nullptr) return;  // a separate merge launch follows
+  // The last CTA of this (row, KV head) merges all splits.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(P.counters + static_cast<long long>(row) * P.hkv + kvh, 1u);
+    s_last = prev == static_cast<unsigned>(P.splits - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  merge8(P, row, hq, d0);
+  if (threadIdx.x == 0) P.counters[static_cast<long long>(row) * P.hkv + kvh] = 0u;
 }
 
 // Log-sum-exp merge of the split partials, then bf16 rounding and the gate.
 __global__ void __launch_bounds__(256) gqa_merge_kernel(const GqaParams P) {
   const int row = blockIdx.x;
-  for (int idx = threadIdx.x; idx < P.hq * 16; idx += blockDim.x) {
-    const int hq = idx >> 4, d0 = (idx & 15) * 8;
-    float M = -INFINITY;
-    for (int s = 0; s < P.splits; ++s)
-      M = fmaxf(M, P.part_lse[(static_cast<long long>(s) * P.rows + row) * P.hq + hq]);
-    float W = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < P.splits; ++s) {
-      const long long pb = (static_cast<long long>(s) * P.rows + row) * P.hq + hq;
-      const float lse = P.part_lse[pb];
-      if (lse == -INFINITY) continue;
-      const float wt = exp2f(lse - M);
-      W += wt;
-      const float4* po = reinterpret_cast<const float4*>(P.part_o + pb * 128 + d0);
-      const float4 a = po[0], b = po[1];
-      acc[0] += wt * a.x; acc[1] += wt * a.y; acc[2] += wt * a.z; acc[3] += wt * a.w;
-      acc[4] += wt * b.x; acc[5] += wt * b.y; acc[6] += wt * b.z; acc[7] += wt * b.w;
-    }
-    const float inv = W > 0.f ? 1.0f / W : 0.f;
-    const long long obase = (static_cast<long long>(row) * P.hq + hq) * 128 + d0;
-    float gv[8];
-    if (P.gate != nullptr) {
-      const uint4 gr = *reinterpret_cast<const uint4*>(P.gate + obase);
-      gv[0] = bf16_lo(gr.x); gv[1] = bf16_hi(gr.x); gv[2] = bf16_lo(gr.y); gv[3] = bf16_hi(gr.y);
-      gv[4] = bf16_lo(gr.z); gv[5] = bf16_hi(gr.z); gv[6] = bf16_lo(gr.w); gv[7] = bf16_hi(gr.w);
-    }
-    float y[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      y[e] = bf16_round(acc[e] * inv);
-      if (P.gate != nullptr) y[e] = y[e] * sigmoidf_(gv[e]);
-    }
-    uint4 ov;
-    ov.x = pack_bf16x2(y[0], y[1]);
-    ov.y = pack_bf16x2(y[2], y[3]);
-    ov.z = pack_bf16x2(y[4], y[5]);
-    ov.w = pack_bf16x2(y[6], y[7]);
-    *reinterpret_cast<uint4*>(P.out + obase) = ov;
-  }
+  for (int idx = threadIdx.x; idx < P.hq * 16; idx += blockDim.x) merge8(P, row, idx >> 4, (idx & 15) * 8);
 }
 
 }  // namespace
 
-// Split-KV count: enough CTAs to cover the SMs about twice, never more
-// splits than 64-token tiles.
+// Split-KV count: at least one CTA per SM, and no CTA with more than
+// kMaxTiles 64-token tiles (its row ids are staged in shared memory).
 int gqa_num_splits(int rows, int hkv, int packed_width) {
   const long long base = static_cast<long long>(rows) * hkv;
   if (base <= 0) return 1;
   const int max_tiles = (packed_width - 1 + kTile - 1) / kTile;
-  const long long target = 2 * 152 * 2;
-  long long s = (target + base - 1) / base;
+  const int min_s = (max_tiles + kMaxTiles - 1) / kMaxTiles;
+  long long s = (152 + base - 1) / base;
   if (s > max_tiles) s = max_tiles;
-  if (s > 32) s = 32;
+  if (s > 64) s = 64;
+  if (s < min_s) s = min_s;
   if (s < 1) s = 1;
   return static_cast<int>(s);
 }
 
 cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e != cudaSuccess) return e;
+  if (static_cast<long long>(p.num_blocks) * p.hkv * p.page >= static_cast<long long>(kBadRow))
+    return cudaErrorInvalidValue;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  if (p.splits > 1 && p.counters != nullptr) {
+    cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(unsigned) * p.rows * p.hkv, stream);
+    if (e != cudaSuccess) return e;
+  }
   gqa_kernel<<<dim3(p.rows * p.hkv, p.splits), 128, kSmem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || p.splits == 1) return e;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1 || p.counters != nullptr) return e;
   gqa_merge_kernel<<<p.rows, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }

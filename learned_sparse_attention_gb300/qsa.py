@@ -84,6 +84,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qsa_check_errors": [ctypes.POINTER(ctypes.c_int64)],
         "qsa_version": [],
         "qsa_step_launches": [P, P, I, I, I],
+        "qsa_gqa_splits": [P, I, I],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -262,6 +263,11 @@ def step_launches(cfg, gcfg, rows, reqs, skip_topk=False) -> int:
     """Kernel launches made by one layer_step call."""
     return int(load().qsa_step_launches(ctypes.byref(cfg), ctypes.byref(gcfg), rows, reqs,
                                         1 if skip_topk else 0))
+
+
+def gqa_splits(gcfg, rows, packed_width) -> int:
+    """Split-KV factor of the sparse GQA stage for these sizes."""
+    return int(load().qsa_gqa_splits(ctypes.byref(gcfg), rows, packed_width))
 
 
 def check_errors() -> int:

@@ -22,10 +22,11 @@ from tests.parity import close_bf16
 pytestmark = pytest.mark.gpu
 
 
-def _case(rows, hkv, seed):
-    spec = W.small_spec("noalloc", seed=seed, contexts=[3000 + 997 * i for i in range(rows)],
+def _case(rows, hkv, seed, ratio=4, topk=2048, contexts=None):
+    contexts = contexts or [3000 + 997 * i for i in range(rows)]
+    spec = W.small_spec("noalloc", seed=seed, contexts=contexts,
                         rows_per_req=[1] * rows, n_heads=8, index_dtype=W.DTYPE_BF16,
-                        compress_ratio=4, token_topk=2048, hq=8 * hkv, hkv=hkv, page=64)
+                        compress_ratio=ratio, token_topk=topk, hq=8 * hkv, hkv=hkv, page=64)
     wl = W.make_workload(spec, device="cuda")
     cfg, gcfg = cfgs(spec, wl)
     return spec, wl, cfg, gcfg
@@ -34,7 +35,7 @@ def _case(rows, hkv, seed):
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
     spec, wl, cfg, gcfg = _case(rows=8, hkv=4, seed=31)
     # 8 rows x 4 KV heads: few CTAs, so split-KV (and its scratch) is in use
-    assert Q.step_launches(cfg, gcfg, spec.rows, spec.reqs) == 7
+    assert Q.gqa_splits(gcfg, spec.rows, spec.packed_width) > 1
     st = OracleState(wl, with_kv=False)
     ws = torch.empty(1 << 26, dtype=torch.uint8, device="cuda")
     for call, seed in enumerate((1, 2)):
@@ -56,10 +57,12 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    # 151 rows x 4 KV heads takes two splits: 2 * 151 * 32 * 128 fp32 partials
-    # = 4.9 MB > 4 MiB.  Every row is empty, so nothing would be read even if
-    # the call were (wrongly) launched.
-    spec, wl, cfg, gcfg = _case(rows=151, hkv=4, seed=32)
+    # 100 rows x 8 KV heads with 4103-token selections take two splits:
+    # 2 * 100 * 64 * 128 fp32 partials = 6.6 MB > 4 MiB.  Every row is empty,
+    # so nothing would be read even if the call were (wrongly) launched.
+    spec, wl, cfg, gcfg = _case(rows=100, hkv=8, seed=32, ratio=8, topk=4096,
+                                contexts=[4200] * 100)
+    assert Q.gqa_splits(gcfg, spec.rows, spec.packed_width) == 2
     packed = torch.full((spec.rows, spec.packed_width), -1, dtype=torch.int32, device="cuda")
     packed[:, -1] = 0
     out = torch.empty_like(wl["q"])
