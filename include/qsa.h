@@ -280,9 +280,10 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg,
 size_t qsa_workspace_bytes(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg,
                            int32_t rows, int32_t reqs, int32_t max_visible);
 
-/* Number of kernel launches one qsa_layer_step call makes for these sizes
- * (compress, ring commit, row-group plan, logits, top-k and sparse GQA; 3
- * with skip_topk).  0 if invalid. */
+/* Number of kernel launches one qsa_layer_step call makes for these sizes:
+ * 4 (compress with the logits row-group table, logits, top-k with the ring
+ * commit, sparse GQA with its split merge), or 3 with skip_topk (compress,
+ * ring commit, sparse GQA).  0 if invalid. */
 int32_t qsa_step_launches(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t rows,
                           int32_t reqs, int32_t skip_topk);
 

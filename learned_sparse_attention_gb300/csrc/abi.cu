@@ -148,7 +148,8 @@ qsa_status do_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
                        const int32_t* token_to_req, const int32_t* query_start_loc,
                        const int32_t* logical_positions, void* ccache, int32_t cpages,
                        const int64_t* compressed_slots, int32_t rows, int32_t reqs,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const LogitsParams* plan = nullptr,
+                       bool commit_ring = true, CompressParams* out_params = nullptr) {
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (rows < 0 || reqs < 0) return QSA_ERR_SHAPE;
@@ -200,16 +201,20 @@ qsa_status do_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
   p.eps = cfg->eps;
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
-  st = cuda_status(launch_compress(p, stream));
-  if (st != QSA_OK) return st;
+  if (out_params != nullptr) *out_params = p;
+  st = cuda_status(launch_compress(p, plan, stream));
+  if (st != QSA_OK || !commit_ring) return st;
   return cuda_status(launch_ring_commit(p, stream));
 }
 
-qsa_status do_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache, int32_t cpages,
-                     const int32_t* cblock_table, int32_t cbt_stride, const int32_t* token_to_req,
-                     const int32_t* query_start_loc, const int32_t* logical_positions,
-                     float* logits, int64_t ld, int32_t max_visible, int32_t rows, int32_t reqs,
-                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+// Validates the logits arguments and fills the kernel parameters; the
+// row-group table lives at the start of ws.
+qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccache, int32_t cpages,
+                         const int32_t* cblock_table, int32_t cbt_stride,
+                         const int32_t* token_to_req, const int32_t* query_start_loc,
+                         const int32_t* logical_positions, float* logits, int64_t ld,
+                         int32_t max_visible, int32_t rows, int32_t reqs, void* ws,
+                         size_t ws_bytes, LogitsParams* out, int* npad_out, int* chunks_out) {
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (rows < 0 || reqs < 0 || max_visible < 0) return QSA_ERR_SHAPE;
@@ -222,12 +227,10 @@ qsa_status do_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache, 
     return QSA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(ws) & 255) return QSA_ERR_WORKSPACE;
   if (ws_bytes < logits_ws_bytes(rows, reqs, cfg)) return QSA_ERR_WORKSPACE;
-  (void)token_to_req;
 
   int R, npad;
   logits_grouping(cfg, rows, reqs, &R, &npad);
   const int max_groups = max_groups_for(rows, reqs, R);
-  const int eb = elem_bytes(cfg);
   LogitsParams p{};
   p.cblock_table = cblock_table;
   p.logical = logical_positions;
@@ -248,7 +251,7 @@ qsa_status do_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache, 
   p.ratio = cfg->compress_ratio;
   p.scale = 1.0f / (static_cast<float>(cfg->n_heads) * sqrtf(128.0f));
   p.manual = cfg->cpage < 8 ? 1 : 0;
-  p.row_bytes = 128 * eb;
+  p.row_bytes = 128 * elem_bytes(cfg);
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
 
@@ -258,24 +261,49 @@ qsa_status do_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache, 
   long long tpc = (work + 4 * 152 - 1) / (4 * 152);
   if (tpc < 2) tpc = 2;
   if (tpc > max_tiles) tpc = max_tiles;
+  if (!p.manual && tpc * (128 / cfg->cpage) > 4096) tpc = 4096 / (128 / cfg->cpage);
   p.tiles_per_cta = static_cast<int>(tpc);
-  const int chunks = static_cast<int>((max_tiles + tpc - 1) / tpc);
+  *chunks_out = static_cast<int>((max_tiles + tpc - 1) / tpc);
+  *npad_out = npad;
+  *out = p;
+  return QSA_OK;
+}
 
+qsa_status launch_logits(const qsa_cfg* cfg, const LogitsParams& p, const void* q_idx,
+                         const void* ccache, int32_t rows, int32_t cpages, int npad, int chunks,
+                         bool plan_done, cudaStream_t stream) {
+  const int eb = elem_bytes(cfg);
   CUtensorMap tq, tk;
   if (!encode_rows_map(&tq, q_idx, eb, static_cast<long long>(rows) * cfg->n_heads, npad))
     return QSA_ERR_CUDA;
   const int kbox = p.manual ? 8 : cfg->cpage;
   if (!encode_rows_map(&tk, ccache, eb, static_cast<long long>(cpages) * cfg->cpage, kbox))
     return QSA_ERR_CUDA;
-  st = cuda_status(launch_logits_plan(p, stream));
-  if (st != QSA_OK) return st;
+  if (!plan_done) {
+    qsa_status st = cuda_status(launch_logits_plan(p, stream));
+    if (st != QSA_OK) return st;
+  }
   return cuda_status(
-      launch_index_logits(p, tq, tk, cfg->index_dtype, npad, max_groups, chunks, stream));
+      launch_index_logits(p, tq, tk, cfg->index_dtype, npad, p.max_groups, chunks, stream));
+}
+
+qsa_status do_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache, int32_t cpages,
+                     const int32_t* cblock_table, int32_t cbt_stride, const int32_t* token_to_req,
+                     const int32_t* query_start_loc, const int32_t* logical_positions,
+                     float* logits, int64_t ld, int32_t max_visible, int32_t rows, int32_t reqs,
+                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+  LogitsParams p{};
+  int npad = 0, chunks = 0;
+  qsa_status st = logits_params(cfg, q_idx, ccache, cpages, cblock_table, cbt_stride, token_to_req,
+                                query_start_loc, logical_positions, logits, ld, max_visible, rows,
+                                reqs, ws, ws_bytes, &p, &npad, &chunks);
+  if (st != QSA_OK || rows == 0 || max_visible == 0) return st;
+  return launch_logits(cfg, p, q_idx, ccache, rows, cpages, npad, chunks, false, stream);
 }
 
 qsa_status do_topk(const qsa_cfg* cfg, const float* logits, int64_t ld, int32_t max_visible,
                    const int32_t* logical_positions, int32_t* packed, int32_t rows,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, const CompressParams* ring = nullptr) {
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (rows < 0 || max_visible < 0) return QSA_ERR_SHAPE;
@@ -295,6 +323,10 @@ qsa_status do_topk(const qsa_cfg* cfg, const float* logits, int64_t ld, int32_t 
   p.max_visible = max_visible;
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
+  if (ring != nullptr) {
+    p.do_ring = 1;
+    p.ring = *ring;
+  }
   return cuda_status(launch_topk(p, stream));
 }
 
@@ -434,21 +466,43 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
   if (ws_bytes < L.total) return QSA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  void* q_idx = skip_topk ? nullptr : w + L.q_idx;
-  st = do_compress(cfg, skip_topk ? nullptr : a->projected_q, q_idx, a->raw_keys, a->positions,
-                   a->cos_sin, a->q_norm_w, a->k_norm_w, a->ring, a->ring_blocks, a->ring_pos,
-                   a->ring_block_table, a->ring_bt_stride, a->token_to_req, a->query_start_loc,
-                   a->logical_positions, a->ccache, a->cpages, a->compressed_slots, a->rows,
-                   a->reqs, s);
-  if (st != QSA_OK) return st;
   const int pw = cfg->token_topk + cfg->compress_ratio;
-  if (!skip_topk) {
-    float* logits = reinterpret_cast<float*>(w + L.logits);
-    st = do_logits(cfg, q_idx, a->ccache, a->cpages, a->cblock_table, a->cbt_stride,
-                   a->token_to_req, a->query_start_loc, a->logical_positions, logits, L.ld,
-                   a->max_visible, a->rows, a->reqs, w + L.logits_ws, L.gqa_ws - L.logits_ws, s);
+  if (skip_topk) {
+    // stage 1 only (ring commit included), then stage 4 on the given buffer
+    st = do_compress(cfg, nullptr, nullptr, a->raw_keys, a->positions, a->cos_sin, a->q_norm_w,
+                     a->k_norm_w, a->ring, a->ring_blocks, a->ring_pos, a->ring_block_table,
+                     a->ring_bt_stride, a->token_to_req, a->query_start_loc, a->logical_positions,
+                     a->ccache, a->cpages, a->compressed_slots, a->rows, a->reqs, s);
     if (st != QSA_OK) return st;
-    st = do_topk(cfg, logits, L.ld, a->max_visible, a->logical_positions, a->packed, a->rows, s);
+  } else {
+    void* q_idx = w + L.q_idx;
+    float* logits = reinterpret_cast<float*>(w + L.logits);
+    LogitsParams lp{};
+    int npad = 0, chunks = 0;
+    const bool any_visible = a->max_visible > 0;
+    if (any_visible) {
+      st = logits_params(cfg, q_idx, a->ccache, a->cpages, a->cblock_table, a->cbt_stride,
+                         a->token_to_req, a->query_start_loc, a->logical_positions, logits, L.ld,
+                         a->max_visible, a->rows, a->reqs, w + L.logits_ws,
+                         L.gqa_ws - L.logits_ws, &lp, &npad, &chunks);
+      if (st != QSA_OK) return st;
+    }
+    // stage 1; the same launch builds the logits row-group table
+    CompressParams cp{};
+    st = do_compress(cfg, a->projected_q, q_idx, a->raw_keys, a->positions, a->cos_sin,
+                     a->q_norm_w, a->k_norm_w, a->ring, a->ring_blocks, a->ring_pos,
+                     a->ring_block_table, a->ring_bt_stride, a->token_to_req, a->query_start_loc,
+                     a->logical_positions, a->ccache, a->cpages, a->compressed_slots, a->rows,
+                     a->reqs, s, any_visible ? &lp : nullptr, /*commit_ring=*/false, &cp);
+    if (st != QSA_OK) return st;
+    if (any_visible) {
+      st = launch_logits(cfg, lp, q_idx, a->ccache, a->rows, a->cpages, npad, chunks,
+                         /*plan_done=*/true, s);
+      if (st != QSA_OK) return st;
+    }
+    // stage 3; the same launch commits the ring after every pooling read
+    st = do_topk(cfg, logits, L.ld, a->max_visible, a->logical_positions, a->packed, a->rows, s,
+                 &cp);
     if (st != QSA_OK) return st;
   }
   return do_gqa(gcfg, a->q, a->kv, a->block_table, a->bt_stride, a->packed, pw, a->token_to_req,
@@ -469,7 +523,7 @@ int32_t qsa_step_launches(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t r
   const int pw = cfg->token_topk + cfg->compress_ratio;
   const int splits = gqa_num_splits(rows, gcfg->num_kv_heads, pw);
   (void)splits;  // split-KV partials are merged inside the GQA kernel
-  return 2 + (skip_topk ? 0 : 3) + 1;
+  return skip_topk ? 3 : 4;
 }
 
 int32_t qsa_gqa_splits(const qsa_gqa_cfg* gcfg, int32_t rows, int32_t packed_width) {

@@ -10,11 +10,15 @@
 // MRoPE).  The norm, rotation and cast are fused into one pass in fp32 with a
 // single rounding to the indexer dtype.
 //
-// Layout of the work: one CTA per row, 128 threads = 8 half-warps; a
-// half-warp owns one 128-dim head vector, each lane 8 consecutive dims
-// (one 16-byte load).  RoPE partners (i, i + 32) sit 4 lanes apart.
+// Layout of the work: 128-thread CTAs.  CTA i < rows prepares the query of
+// row i: 8 half-warps, each owning n_heads / 8 head vectors, each lane 8
+// consecutive dims (one 16-byte load per head, all issued before any math);
+// RoPE partners (i, i + 32) sit 4 lanes apart.  CTA rows + i pools the group
+// completed by row i, if any, in parallel with the query CTAs.  An optional
+// last CTA builds the logits kernel's row-group table.
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
+#include "stage_helpers.cuh"
 
 namespace qsa {
 namespace {
@@ -41,6 +45,18 @@ __device__ __forceinline__ void rope_coeffs(const CompressParams& P, int lane16,
                                             const int64_t (&pos)[3], float (&c)[8],
                                             float (&s)[8]) {
   const int fbase = 8 * (lane16 & 3);
+  if (!P.mrope) {
+    int64_t pp = pos[0];
+    if (pp < 0 || pp >= P.max_pos) {
+      if (lane16 == 0) flag_error(P.err);
+      pp = pp < 0 ? 0 : P.max_pos - 1;
+    }
+    const float4* row = reinterpret_cast<const float4*>(P.cos_sin + pp * 64 + fbase);
+    const float4 c0 = row[0], c1 = row[1], s0 = row[8], s1 = row[9];
+    c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w; c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+    s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w; s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+    return;
+  }
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int i = fbase + e;
@@ -99,19 +115,34 @@ __device__ __forceinline__ void store8(void* base, long long elem_off, const flo
 }
 
 template <int IDT>
-__global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
-  const int row = blockIdx.x;
+__global__ void __launch_bounds__(128) compress_kernel(const CompressParams P, const LogitsParams L,
+                                                       int do_plan) {
+  const int b = blockIdx.x;
+  if (b >= 2 * P.rows) {  // the logits kernel's row-group table
+    if (do_plan) plan_groups(L);
+    return;
+  }
+  const bool pool = b >= P.rows;
+  const int row = pool ? b - P.rows : b;
   const int hw = threadIdx.x >> 4;       // half-warp 0..7
   const int lane16 = threadIdx.x & 15;   // dims 8*lane16 .. +7
   const int req = P.token_to_req[row];
   const int p = P.logical[row];
   if (req < 0 || req >= P.reqs) {
-    if (threadIdx.x == 0) flag_error(P.err);
+    if (pool && threadIdx.x == 0) flag_error(P.err);
     return;
   }
 
-  // ---- indexer query: every head of this row
-  if (P.projected_q != nullptr) {
+  if (!pool) {
+    // ---- indexer query: every head of this row, all loads issued first
+    if (P.projected_q == nullptr) return;
+    const int nh = P.n_heads >> 3;  // heads per half-warp: 1, 2, 4 or 8
+    float x[8][8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < nh)
+        load8_bf16(P.projected_q + (static_cast<long long>(row) * P.n_heads + hw + 8 * k) * kD +
+                       8 * lane16, x[k]);
     int64_t pos[3];
 #pragma unroll
     for (int k = 0; k < 3; ++k)
@@ -121,13 +152,15 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
     load8_bf16(P.q_norm_w + 8 * lane16, w1);
 #pragma unroll
     for (int e = 0; e < 8; ++e) w1[e] += 1.0f;
-    for (int h = hw; h < P.n_heads; h += 8) {
-      const long long off = (static_cast<long long>(row) * P.n_heads + h) * kD + 8 * lane16;
-      float x[8];
-      load8_bf16(P.projected_q + off, x);
-      norm_rope(x, w1, P.eps, lane16, c, s);
-      store8<IDT>(P.q_idx, off, x);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k < nh) {
+        norm_rope(x[k], w1, P.eps, lane16, c, s);
+        store8<IDT>(P.q_idx,
+                    (static_cast<long long>(row) * P.n_heads + hw + 8 * k) * kD + 8 * lane16, x[k]);
+      }
     }
+    return;
   }
 
   // ---- group completed by this row: pool, norm, rotate, cast, store.
@@ -188,35 +221,22 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
 // sequential "later rows overwrite earlier rows" result without races.
 __global__ void __launch_bounds__(128) ring_commit_kernel(const CompressParams P) {
   const int row = blockIdx.x * 8 + (threadIdx.x >> 4);
-  const int lane16 = threadIdx.x & 15;
-  if (row >= P.rows) return;
-  const int req = P.token_to_req[row];
-  if (req < 0 || req >= P.reqs) return;  // already counted by the compress kernel
-  const int p = P.logical[row];
-  const int p_last = P.logical[P.qsl[req + 1] - 1];
-  if (p + P.S <= p_last) return;  // overwritten later in this step
-  const int ring_block = P.ring_bt[static_cast<long long>(req) * P.ring_bt_stride];
-  if (ring_block < 0 || ring_block >= P.ring_blocks || p < 0) {
-    if (lane16 == 0) flag_error(P.err);
-    return;
-  }
-  const long long ring_slot = static_cast<long long>(ring_block) * P.S + (p % P.S);
-  const uint4 v =
-      *reinterpret_cast<const uint4*>(P.raw_keys + static_cast<long long>(row) * kD + 8 * lane16);
-  *reinterpret_cast<uint4*>(P.ring + ring_slot * kD + 8 * lane16) = v;
-  if (P.ring_pos != nullptr && lane16 < 3) {
-    P.ring_pos[ring_slot * 3 + lane16] = P.positions[static_cast<long long>(row) * 3 + lane16];
-  }
+  if (row < P.rows) ring_commit_row(P, row, threadIdx.x & 15);
 }
 
 }  // namespace
 
-cudaError_t launch_compress(const CompressParams& p, cudaStream_t stream) {
+cudaError_t launch_compress(const CompressParams& p, const LogitsParams* plan,
+                            cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;
+  LogitsParams L{};
+  if (plan != nullptr) L = *plan;
+  const int grid = 2 * p.rows + (plan != nullptr ? 1 : 0);
+  const int do_plan = plan != nullptr ? 1 : 0;
   if (p.index_dtype == 1)
-    compress_kernel<1><<<p.rows, 128, 0, stream>>>(p);
+    compress_kernel<1><<<grid, 128, 0, stream>>>(p, L, do_plan);
   else
-    compress_kernel<0><<<p.rows, 128, 0, stream>>>(p);
+    compress_kernel<0><<<grid, 128, 0, stream>>>(p, L, do_plan);
   return cudaGetLastError();
 }
 

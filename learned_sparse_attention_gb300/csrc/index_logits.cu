@@ -20,6 +20,7 @@
 // Every wait is bounded (see mbar_wait); a timeout sets the error word.
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
+#include "stage_helpers.cuh"
 
 namespace qsa {
 namespace {
@@ -36,61 +37,11 @@ struct LogitsCfg {
   static constexpr int THREADS = 64 + 128 * EPI_WG;
   static constexpr int KSTEPS = IDT == 1 ? 4 : 8;       // 32 bytes of K per MMA
   static constexpr uint32_t TMEM_COLS = 2 * NPAD;
-  static constexpr int SMEM = 1024 + STAGES * A_STAGE + B_BYTES + 256;
+  static constexpr int MAX_PAGES = 4096;                // page ids staged per CTA
+  static constexpr int SMEM = 1024 + STAGES * A_STAGE + B_BYTES + 256 + MAX_PAGES * 4 + 32 * 4;
 };
 
-__global__ void __launch_bounds__(1024) logits_plan_kernel(const LogitsParams P) {
-  __shared__ int warp_tot[32];
-  __shared__ int carry;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) carry = 0;
-  __syncthreads();
-  const int R = P.rows_per_group;
-  for (int base = 0; base < P.reqs; base += 1024) {
-    const int q = base + tid;
-    int n = 0, start = 0;
-    if (q < P.reqs) {
-      start = P.qsl[q];
-      n = P.qsl[q + 1] - start;
-      if (n < 0) {
-        flag_error(P.err);
-        n = 0;
-      }
-    }
-    const int ng = (n + R - 1) / R;
-    int incl = ng;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      int v = warp_tot[lane];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += y;
-      }
-      warp_tot[lane] = v;
-    }
-    __syncthreads();
-    const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - ng;
-    for (int k = 0; k < ng; ++k) {
-      const int idx = excl + k;
-      if (idx >= P.max_groups) {
-        flag_error(P.err);
-        break;
-      }
-      P.groups[idx] = make_int4(start + k * R, min(R, n - k * R), q, 0);
-    }
-    __syncthreads();
-    if (tid == 0) carry += warp_tot[31];
-    __syncthreads();
-  }
-  if (tid == 0) *P.group_count = min(carry, P.max_groups);
-}
+__global__ void __launch_bounds__(1024) logits_plan_kernel(const LogitsParams P) { plan_groups(P); }
 
 template <int IDT, int NPAD>
 __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
@@ -119,8 +70,30 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* bar_q = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 1);
+  int* s_page = reinterpret_cast<int*>(smem_raw + pad + C::STAGES * C::A_STAGE + C::B_BYTES + 256);
+  int* s_vis = s_page + C::MAX_PAGES;  // visible blocks of the group's rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cpage = P.cpage;
+  const int32_t* bt_row = P.cblock_table + static_cast<long long>(req) * P.cbt_stride;
+  // Prologue: the group's visible-block counts and the physical compressed
+  // pages of this CTA's key range, resolved in parallel before any copy.
+  const int ppt = P.manual ? 0 : 128 / cpage;  // pages per 128-key tile
+  const int page0 = t_begin * ppt;
+  const int npages = min(ntiles * ppt, C::MAX_PAGES);
+  const int last_page = min((vmax - 1) / cpage, P.cbt_stride - 1);
+  for (int i = threadIdx.x; i < npages; i += blockDim.x) {
+    int phys = bt_row[min(page0 + i, last_page)];
+    if (phys < 0 || phys >= P.cpages) {
+      flag_error(P.err);
+      phys = 0;
+    }
+    s_page[i] = phys;
+  }
+  for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
+    const int pr = P.logical[row0 + r];
+    s_vis[r] = pr < 0 ? 0 : (pr + 1) / P.ratio;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -142,7 +115,6 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   unsigned long long* err = P.err;
-  const int cpage = P.cpage;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -154,8 +126,6 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
       for (int atom = 0; atom < C::ATOMS; ++atom)
         tma_load_2d(sB + atom * C::B_ATOM, &tmap_q, atom * 64, row0 * P.n_heads, bar_q);
     }
-    const int last_page = (vmax - 1) / cpage;
-    const int32_t* bt_row = P.cblock_table + static_cast<long long>(req) * P.cbt_stride;
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % C::STAGES;
       const uint32_t ph = (i / C::STAGES) & 1;
@@ -167,13 +137,7 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
         if (lane == 0) mbar_arrive_expect_tx(&full[s], C::A_STAGE);
         __syncwarp();
         for (int pg = lane; pg < pages; pg += 32) {
-          int lp = min(tile * pages + pg, last_page);
-          lp = min(lp, P.cbt_stride - 1);
-          int phys = bt_row[lp];
-          if (phys < 0 || phys >= P.cpages) {
-            flag_error(err);
-            phys = 0;
-          }
+          const int phys = s_page[min(i * pages + pg, npages - 1)];
 #pragma unroll
           for (int atom = 0; atom < C::ATOMS; ++atom)
             tma_load_2d(dst + atom * C::A_ATOM + pg * cpage * 128, &tmap_k, atom * 64,
@@ -264,11 +228,8 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
           sum += fmaxf(v[j], 0.f);
           if (((col + 1) & hmask) == 0) {
             const int r = col / P.n_heads;
-            if (r < nrows) {
-              const int row = row0 + r;
-              const int V = (P.logical[row] + 1) / P.ratio;
-              if (key < V) P.logits[static_cast<long long>(row) * P.ld + key] = sum * P.scale;
-            }
+            if (r < nrows && key < s_vis[r])
+              P.logits[static_cast<long long>(row0 + r) * P.ld + key] = sum * P.scale;
             sum = 0.f;
           }
         }

@@ -31,7 +31,10 @@ struct CompressParams {
   unsigned long long* err;
 };
 
-cudaError_t launch_compress(const CompressParams& p, cudaStream_t stream);
+struct LogitsParams;
+
+// plan: when non-null, the same launch also builds the logits row-group table.
+cudaError_t launch_compress(const CompressParams& p, const LogitsParams* plan, cudaStream_t stream);
 cudaError_t launch_ring_commit(const CompressParams& p, cudaStream_t stream);
 
 struct LogitsParams {
@@ -67,6 +70,8 @@ struct TopkParams {
   int32_t* packed;
   int rows, ratio, token_topk, max_visible;
   unsigned long long* err;
+  int do_ring;            // also commit the step's raw keys to the ring
+  CompressParams ring;
 };
 size_t topk_smem_bytes(int max_visible, int block_topk);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);

@@ -1,0 +1,92 @@
+// Block-level pieces shared by several kernels of the layer step so that small
+// jobs ride along in a neighbouring launch instead of a launch of their own:
+// the ring commit (stage 1 bookkeeping, done by the top-k launch) and the
+// row-group table of the logits kernel (built by the compress launch).
+#pragma once
+
+#include "qsa_device.cuh"
+#include "qsa_kernels.h"
+
+namespace qsa {
+
+// Ring commit of one row by 16 lanes: the row's raw key (and 3-D position)
+// goes to ring slot p % S of its request, unless a later row of the same
+// request in this step maps to the same slot.  Must run after every pooling
+// read of the step.
+__device__ __forceinline__ void ring_commit_row(const CompressParams& P, int row, int lane16) {
+  const int req = P.token_to_req[row];
+  if (req < 0 || req >= P.reqs) return;  // counted by the compress kernel
+  const int p = P.logical[row];
+  const int p_last = P.logical[P.qsl[req + 1] - 1];
+  if (p + P.S <= p_last) return;  // overwritten later in this step
+  const int ring_block = P.ring_bt[static_cast<long long>(req) * P.ring_bt_stride];
+  if (ring_block < 0 || ring_block >= P.ring_blocks || p < 0) {
+    if (lane16 == 0) flag_error(P.err);
+    return;
+  }
+  const long long ring_slot = static_cast<long long>(ring_block) * P.S + (p % P.S);
+  const uint4 v =
+      *reinterpret_cast<const uint4*>(P.raw_keys + static_cast<long long>(row) * 128 + 8 * lane16);
+  *reinterpret_cast<uint4*>(P.ring + ring_slot * 128 + 8 * lane16) = v;
+  if (P.ring_pos != nullptr && lane16 < 3)
+    P.ring_pos[ring_slot * 3 + lane16] = P.positions[static_cast<long long>(row) * 3 + lane16];
+}
+
+// Row-group table of the logits kernel: each request's rows in chunks of
+// rows_per_group, in request order.  Executed by one whole block (any size
+// that is a multiple of 32, at most 1024 threads).
+__device__ __forceinline__ void plan_groups(const LogitsParams& P) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  const int R = P.rows_per_group;
+  for (int base = 0; base < P.reqs; base += blockDim.x) {
+    const int q = base + tid;
+    int n = 0, start = 0;
+    if (q < P.reqs) {
+      start = P.qsl[q];
+      n = P.qsl[q + 1] - start;
+      if (n < 0) {
+        flag_error(P.err);
+        n = 0;
+      }
+    }
+    const int ng = (n + R - 1) / R;
+    int incl = ng;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int v = lane < nwarps ? warp_tot[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += y;
+      }
+      if (lane < nwarps) warp_tot[lane] = v;
+    }
+    __syncthreads();
+    const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - ng;
+    for (int k = 0; k < ng; ++k) {
+      const int idx = excl + k;
+      if (idx >= P.max_groups) {
+        flag_error(P.err);
+        break;
+      }
+      P.groups[idx] = make_int4(start + k * R, min(R, n - k * R), q, 0);
+    }
+    __syncthreads();
+    if (tid == 0) carry += warp_tot[nwarps - 1];
+    __syncthreads();
+  }
+  if (tid == 0) *P.group_count = min(carry, P.max_groups);
+}
+
+}  // namespace qsa

@@ -8,13 +8,16 @@
 // = valid count.
 //
 // One CTA of 1024 threads per row.  The row's V logits are staged in shared
-// memory as order-preserving 32-bit keys; a 4-pass, 8-bit radix select finds
-// the K_b-th largest key T and how many keys equal to T are taken; a
+// memory as order-preserving 32-bit keys; an 8-bit radix select, starting
+// below the bits that the row's smallest and largest keys share and with
+// warp-aggregated histogram atomics, finds the K_b-th largest key T and how
+// many keys equal to T are taken; a
 // block-wide scan then writes the selected block ids in ascending order, the
 // lower block winning among equal keys.  Rows with V <= K_b select every
 // visible block without reading logits.
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
+#include "stage_helpers.cuh"
 
 namespace qsa {
 namespace {
@@ -90,16 +93,67 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
   const bool take_all = V <= kb;
   if (!take_all) {
     const float* lrow = P.logits + static_cast<long long>(row) * P.ld;
-    for (int c = tid; c < V; c += kThreads) keys[c] = order_key(lrow[c]);
-
-    uint32_t prefix = 0, pmask = 0;
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    for (int c = tid; c < V; c += kThreads) {
+      const uint32_t key = order_key(lrow[c]);
+      keys[c] = key;
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+    }
+    // Bits above the highest bit where the row's smallest and largest keys
+    // differ are common to every key: the radix passes start below them.
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+    }
+    if ((tid & 31) == 0) {
+      wa[tid >> 5] = static_cast<int>(kmin);
+      wb[tid >> 5] = static_cast<int>(kmax);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      kmin = static_cast<uint32_t>(wa[tid]);
+      kmax = static_cast<uint32_t>(wb[tid]);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
+        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+      }
+      if (tid == 0) {
+        s_digit = static_cast<int>(kmin);
+        s_k = static_cast<int>(kmax);
+      }
+    }
+    __syncthreads();
+    kmin = static_cast<uint32_t>(s_digit);
+    kmax = static_cast<uint32_t>(s_k);
+    __syncthreads();
+    const uint32_t diff = kmin ^ kmax;
+    int hi = diff ? 31 - __clz(diff) : -1;  // highest differing bit
+    uint32_t prefix = hi >= 31 ? 0u : (kmin & ~((2u << hi) - 1u));
+    uint32_t pmask = hi >= 31 ? 0u : ~((2u << hi) - 1u);
+    if (hi < 0) {  // every key equal
+      prefix = kmin;
+      pmask = 0xFFFFFFFFu;
+    }
     int k = kb;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    while (hi >= 0) {
+      const int width = hi + 1 < 8 ? hi + 1 : 8;
+      const int shift = hi - width + 1;
+      const uint32_t dmask = (1u << width) - 1u;
       if (tid < 256) hist[tid] = 0;
       __syncthreads();
       for (int c = tid; c < V; c += kThreads) {
         const uint32_t key = keys[c];
-        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+        const bool in = (key & pmask) == prefix;
+        const int bin = in ? static_cast<int>((key >> shift) & dmask) : -1;
+        // lanes of a warp that fall in the same bin add once
+        const unsigned active = __ballot_sync(__activemask(), in);
+        if (in) {
+          const unsigned same = __match_any_sync(active, bin);
+          if ((threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
+        }
       }
       __syncthreads();
       if (tid < 32) {
@@ -128,17 +182,18 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
       }
       __syncthreads();
       prefix |= static_cast<uint32_t>(s_digit) << shift;
-      pmask |= 255u << shift;
+      pmask |= dmask << shift;
       k = s_k;
+      hi = shift - 1;
       __syncthreads();
     }
     const uint32_t T = prefix;
     const int keq = k;
 
     const int per = (V + kThreads - 1) / kThreads;
-    const int lo = min(V, tid * per), hi = min(V, lo + per);
+    const int lo = min(V, tid * per), hi_end = min(V, lo + per);
     int gt = 0, eq = 0;
-    for (int c = lo; c < hi; ++c) {
+    for (int c = lo; c < hi_end; ++c) {
       const uint32_t key = keys[c];
       gt += key > T;
       eq += key == T;
@@ -147,7 +202,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
     block_scan2(gt, eq, gt_ex, eq_ex, wa, wb);
     int out = gt_ex + min(eq_ex, keq);
     int eq_seen = eq_ex;
-    for (int c = lo; c < hi; ++c) {
+    for (int c = lo; c < hi_end; ++c) {
       const uint32_t key = keys[c];
       if (key > T) {
         sel[out++] = c;
@@ -174,6 +229,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
     prow[idx] = v;
   }
   if (tid == 0) prow[W] = count;
+  // Inside the layer step this launch also commits the row's raw key to the
+  // compressor-state ring (all pooling reads of the step are done by now).
+  if (P.do_ring && tid >= 32 && tid < 48) ring_commit_row(P.ring, row, tid - 32);
 }
 
 }  // namespace
