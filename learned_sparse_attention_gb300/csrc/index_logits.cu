@@ -211,31 +211,55 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
     const int cols = nrows * P.n_heads;
     const int col_begin = wg * (NPAD / C::EPI_WG);
     const int col_end = min(cols, col_begin + NPAD / C::EPI_WG);
-    const int hmask = P.n_heads - 1;
+    constexpr int COLS = NPAD / C::EPI_WG;  // accumulator columns of this warpgroup
     for (int i = 0; i < ntiles; ++i) {
       const int a = i & 1;
       const uint32_t aph = (i >> 1) & 1;
       if (!mbar_wait(&acc_full[a], aph, err)) break;
       tc_fence_after_sync();
       const int key = (t_begin + i) * 128 + m;
-      float sum = 0.f;
-      for (int c0 = col_begin; c0 < col_end; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem_base + (static_cast<uint32_t>(lane_base) << 16) + a * NPAD + c0, v);
+      // One wide TMEM read of the warpgroup's columns, then the accumulator
+      // goes straight back to the MMA warp; sums and stores follow.
+      float v[COLS];
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_base) << 16) + a * NPAD + col_begin;
+      if constexpr (COLS == 32) tmem_ld32(taddr, v);
+      else if constexpr (COLS == 64) tmem_ld64_wait(taddr, v);
+      else tmem_ld128_wait(taddr, v);
+      tc_fence_before_sync();
+      mbar_arrive_relaxed(&acc_empty[a]);
+      // ReLU sums of 8-column segments, then a pairwise tree up to n_heads
+      // columns per row (n_heads is 8, 16, 32 or 64): branch-free, compact.
+      constexpr int NSEG = COLS / 8;
+      float seg[NSEG];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int col = c0 + j;
-          sum += fmaxf(v[j], 0.f);
-          if (((col + 1) & hmask) == 0) {
-            const int r = col / P.n_heads;
-            if (r < nrows && key < s_vis[r])
-              P.logits[static_cast<long long>(row0 + r) * P.ld + key] = sum * P.scale;
-            sum = 0.f;
-          }
+      for (int q = 0; q < NSEG; ++q) {
+        float t = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t += fmaxf(v[q * 8 + e], 0.f);
+        seg[q] = t;
+      }
+      if (P.n_heads >= 16) {
+#pragma unroll
+        for (int q = 0; q < NSEG / 2; ++q) seg[q] = seg[2 * q] + seg[2 * q + 1];
+      }
+      if (P.n_heads >= 32) {
+#pragma unroll
+        for (int q = 0; q < NSEG / 4; ++q) seg[q] = seg[2 * q] + seg[2 * q + 1];
+      }
+      if (P.n_heads >= 64) {
+#pragma unroll
+        for (int q = 0; q < NSEG / 8; ++q) seg[q] = seg[2 * q] + seg[2 * q + 1];
+      }
+      const int rows_here = max(0, col_end - col_begin) / P.n_heads;
+      const int r0 = col_begin / P.n_heads;
+#pragma unroll
+      for (int q = 0; q < NSEG; ++q) {
+        if (q < rows_here) {
+          const int r = r0 + q;
+          if (r < nrows && key < s_vis[r])
+            P.logits[static_cast<long long>(row0 + r) * P.ld + key] = seg[q] * P.scale;
         }
       }
-      tc_fence_before_sync();
-      mbar_arrive(&acc_empty[a]);
     }
   }
   tc_fence_before_sync();

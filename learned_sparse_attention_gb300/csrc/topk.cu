@@ -234,6 +234,220 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
   if (P.do_ring && tid >= 32 && tid < 48) ring_commit_row(P.ring, row, tid - 32);
 }
 
+
+// ---------------------------------------------------------------------------
+// Register variant for V <= kRegKeys * kRegThreads (16384): thread t owns the
+// 32 consecutive blocks [32t, 32t + 32) and keeps their keys in registers.
+// Radix passes use per-warp private histograms (no cross-warp atomics); the
+// final selection is a per-thread bit mask, so the ordered compaction is one
+// block scan of popcounts, ties going to the lower block by construction.
+constexpr int kRegThreads = 512;
+constexpr int kRegKeys = 32;
+constexpr int kRegWarps = kRegThreads / 32;
+
+__device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int x = lane < kRegWarps ? scratch[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane < kRegWarps) scratch[lane] = x;
+  }
+  __syncthreads();
+  const int ex = (warp > 0 ? scratch[warp - 1] : 0) + incl - v;
+  *total = scratch[kRegWarps - 1];
+  __syncthreads();
+  return ex;
+}
+
+__global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams P) {
+  __shared__ int whist[kRegWarps][256];
+  __shared__ int sel[kRegKeys * kRegThreads / 4];  // K_b <= V / ... bounded by token_topk / r
+  __shared__ int scratch[32];
+  __shared__ uint32_t s_min[kRegWarps], s_max[kRegWarps];
+  __shared__ int s_digit, s_k;
+
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = P.ratio;
+  const int kb = P.token_topk / r;
+  const int W = P.token_topk + r - 1;
+  int p = P.logical[row];
+  if (p < -1) {
+    if (tid == 0) flag_error(P.err);
+    p = -1;
+  }
+  int V = (p + 1) / r;
+  if (V > P.max_visible) {
+    if (tid == 0) flag_error(P.err);
+    V = P.max_visible;
+    p = V * r - 1;
+  }
+  const bool take_all = V <= kb;
+  if (!take_all) {
+    // keys of blocks [32 tid, 32 tid + 32); 0 marks "beyond V" (no real score maps to 0)
+    const int base = tid * kRegKeys;
+    const float* lrow = P.logits + static_cast<long long>(row) * P.ld;
+    uint32_t key[kRegKeys];
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+    for (int j = 0; j < kRegKeys; j += 4) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (base + j + 3 < V) v = *reinterpret_cast<const float4*>(lrow + base + j);
+      else {
+        if (base + j < V) v.x = lrow[base + j];
+        if (base + j + 1 < V) v.y = lrow[base + j + 1];
+        if (base + j + 2 < V) v.z = lrow[base + j + 2];
+      }
+      const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool ok = base + j + u < V;
+        key[j + u] = ok ? order_key(f[u]) : 0u;
+        if (ok) {
+          kmin = min(kmin, key[j + u]);
+          kmax = max(kmax, key[j + u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+    }
+    if (lane == 0) {
+      s_min[warp] = kmin;
+      s_max[warp] = kmax;
+    }
+    __syncthreads();
+    kmin = 0xFFFFFFFFu;
+    kmax = 0u;
+#pragma unroll
+    for (int w = 0; w < kRegWarps; ++w) {
+      kmin = min(kmin, s_min[w]);
+      kmax = max(kmax, s_max[w]);
+    }
+    const uint32_t diff = kmin ^ kmax;
+    int hi = diff ? 31 - __clz(diff) : -1;
+    uint32_t prefix, pmask;
+    if (hi < 0) {
+      prefix = kmin;
+      pmask = 0xFFFFFFFFu;
+    } else if (hi == 31) {
+      prefix = 0u;
+      pmask = 0u;
+    } else {
+      pmask = ~((2u << hi) - 1u);
+      prefix = kmin & pmask;
+    }
+    int k = kb;
+    while (hi >= 0) {
+      const int width = hi + 1 < 8 ? hi + 1 : 8;
+      const int shift = hi - width + 1;
+      const uint32_t dmask = (1u << width) - 1u;
+      for (int i = lane; i < 256; i += 32) whist[warp][i] = 0;
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < kRegKeys; ++j) {
+        const bool in = key[j] != 0u && (key[j] & pmask) == prefix;
+        const int bin = in ? static_cast<int>((key[j] >> shift) & dmask) : -1;
+        const unsigned act = __ballot_sync(0xffffffffu, in);
+        if (in) {
+          const unsigned same = __match_any_sync(act, bin);
+          if (lane == __ffs(same) - 1) whist[warp][bin] += __popc(same);
+        }
+        __syncwarp();
+      }
+      __syncthreads();
+      if (tid < 256) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kRegWarps; ++w) c += whist[w][tid];
+        whist[0][tid] = c;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        int cnt[8], tot = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          cnt[j] = whist[0][255 - 8 * lane - j];
+          tot += cnt[j];
+        }
+        int incl = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        int cum = incl - tot;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cum < k && k <= cum + cnt[j]) {
+            s_digit = 255 - 8 * lane - j;
+            s_k = k - cum;
+          }
+          cum += cnt[j];
+        }
+      }
+      __syncthreads();
+      prefix |= static_cast<uint32_t>(s_digit) << shift;
+      pmask |= dmask << shift;
+      k = s_k;
+      hi = shift - 1;
+    }
+    const uint32_t T = prefix;
+    const int keq = k;
+    uint32_t gt_mask = 0u, eq_mask = 0u;
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) {
+      gt_mask |= (key[j] > T ? 1u : 0u) << j;
+      eq_mask |= (key[j] == T ? 1u : 0u) << j;
+    }
+    int tot;
+    const int eq_before = block_sum_excl(__popc(eq_mask), scratch, &tot);
+    // keep the first keq equal keys in block order
+    int take = keq - eq_before;
+    take = take < 0 ? 0 : take;
+    uint32_t eq_take = eq_mask;
+    for (int c = __popc(eq_mask); c > take; --c) eq_take &= ~(1u << (31 - __clz(eq_take)));
+    uint32_t m = gt_mask | eq_take;
+    int out = block_sum_excl(__popc(m), scratch, &tot);
+    while (m) {
+      const int j = __ffs(m) - 1;
+      sel[out++] = base + j;
+      m &= m - 1u;
+    }
+    __syncthreads();
+  }
+
+  const int nsel = take_all ? V : kb;
+  const int tail0 = V * r;
+  const int count = nsel * r + (p + 1 - tail0);
+  int32_t* prow = P.packed + static_cast<long long>(row) * (W + 1);
+  for (int idx = tid; idx < W; idx += kRegThreads) {
+    int v = -1;
+    if (idx < nsel * r) {
+      const int b = take_all ? idx / r : sel[idx / r];
+      v = b * r + idx % r;
+    } else if (idx < count) {
+      v = tail0 + (idx - nsel * r);
+    }
+    prow[idx] = v;
+  }
+  if (tid == 0) prow[W] = count;
+  if (P.do_ring && tid >= 32 && tid < 48) ring_commit_row(P.ring, row, tid - 32);
+}
+
 }  // namespace
 
 size_t topk_smem_bytes(int max_visible, int block_topk) {
@@ -242,6 +456,10 @@ size_t topk_smem_bytes(int max_visible, int block_topk) {
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;
+  if (p.max_visible <= kRegKeys * kRegThreads && p.token_topk / p.ratio <= kRegKeys * kRegThreads / 4) {
+    topk_reg_kernel<<<p.rows, kRegThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   const size_t smem = topk_smem_bytes(p.max_visible, p.token_topk / p.ratio);
   cudaError_t e =
       cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

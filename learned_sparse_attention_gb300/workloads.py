@@ -155,7 +155,8 @@ def _randn(gen, shape, device, dtype=torch.bfloat16, std=1.0):
     return x.to(dtype)
 
 
-def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0, with_caches: bool = True) -> Workload:
+def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0, with_caches: bool = True,
+                  with_kv: bool = True) -> Workload:
     """Build every input of one layer step.  Metadata and small tensors come
     from a CPU generator seeded by (seed, step); the large caches from a
     generator on ``device`` seeded by seed (so they do not depend on step).
@@ -256,14 +257,15 @@ def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0, with_caches: 
         t = {k: v.to(dev) for k, v in t.items() if k != "ring"}
         return Workload(spec, t, image_start)
     gd = torch.Generator(device=dev).manual_seed(spec.seed * 1000 + 7)
-    t["kv"] = _randn(gd, (n_kv_blocks, spec.hkv, spec.page, 2 * D), dev)
+    # without the main KV cache (index-only studies) a one-block stand-in keeps the keys valid
+    t["kv"] = _randn(gd, (n_kv_blocks if with_kv else 1, spec.hkv, spec.page, 2 * D), dev)
     cc = torch.randn((n_cpages, spec.cpage, 1, D), generator=gd, device=dev, dtype=torch.float32)
     if spec.index_dtype == DTYPE_E4M3:
         t["ccache"] = cc.to(torch.float8_e4m3fn).view(torch.uint8)
     else:
         t["ccache"] = cc.to(torch.bfloat16)
 
-    if spec.peak_frac > 0:
+    if spec.peak_frac > 0 and with_kv:
         gp = np.random.default_rng([spec.seed, 99])
         for req in range(reqs):
             L = spec.contexts[req]
