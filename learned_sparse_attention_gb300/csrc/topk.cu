@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
 // ---------------------------------------------------------------------------
 // Register variant for V <= kRegKeys * kRegThreads (16384): thread t owns the
 // 32 consecutive blocks [32t, 32t + 32) and keeps their keys in registers.
-// Radix passes use per-warp private histograms (no cross-warp atomics); the
+// Radix passes use per-warp private histograms (no cross-warp contention); the
 // final selection is a per-thread bit mask, so the ordered compaction is one
 // block scan of popcounts, ties going to the lower block by construction.
 constexpr int kRegThreads = 512;
@@ -359,14 +359,8 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
       __syncwarp();
 #pragma unroll
       for (int j = 0; j < kRegKeys; ++j) {
-        const bool in = key[j] != 0u && (key[j] & pmask) == prefix;
-        const int bin = in ? static_cast<int>((key[j] >> shift) & dmask) : -1;
-        const unsigned act = __ballot_sync(0xffffffffu, in);
-        if (in) {
-          const unsigned same = __match_any_sync(act, bin);
-          if (lane == __ffs(same) - 1) whist[warp][bin] += __popc(same);
-        }
-        __syncwarp();
+        if (key[j] != 0u && (key[j] & pmask) == prefix)
+          atomicAdd(&whist[warp][(key[j] >> shift) & dmask], 1);
       }
       __syncthreads();
       if (tid < 256) {
