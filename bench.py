@@ -39,6 +39,22 @@ METRIC = "QSA layer decode tokens/s and prefill rows/s at 1 GB300; % of HBM / fp
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 512 << 20
 
+# DRAM bytes per launch of the sparse GQA kernel on the decode batch, from one
+# ncu capture (profiles/decode_batch_kernel_sections.md), keyed by a hash of
+# the kernel sources it was taken on; any other source reports null.
+GQA_TRAFFIC = {"401eff568cd728b4": 270356736 + 3680768}
+GQA_SOURCES = ("learned_sparse_attention_gb300/csrc/sparse_gqa.cu",
+               "learned_sparse_attention_gb300/csrc/qsa_device.cuh")
+
+
+def gqa_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in GQA_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
 
 # --------------------------------------------------------------------------- setup
 def dist_env():
@@ -398,7 +414,9 @@ def run_ours(args):
                        "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)"},
             "roofline": {"bound": "hbm", "kernel": "qsa sparse GQA (stage 4)",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": None,
+                         "frac": achieved / hbm,
+                         "traffic": (GQA_TRAFFIC.get(gqa_source_hash())
+                                     if spec.name == "decode_batch" else None),
                          "peak_source": f"{peak_kind} hbm_gbs",
                          "algorithmic_bytes_per_launch": gqa_bytes,
                          "kernel_ms": gqa_ms},
