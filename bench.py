@@ -12,7 +12,9 @@ qsa_layer_step (all four stages) over that batch.
 N > 1 runs under torchrun as independent replicas (one per GPU, no
 collective on the data path: requests are independent), value = total rows
 of all ranks / max time over ranks.  Between timed steps the L2 is flushed by
-writing a 512 MiB buffer; only the step itself sits between the CUDA events.
+writing a 512 MiB buffer, then reading a separate 256 MiB buffer so that the
+written lines are evicted (and written back) before the step instead of
+during it; only the step itself sits between the CUDA events.
 """
 
 from __future__ import annotations
@@ -38,6 +40,13 @@ from learned_sparse_attention_gb300 import workloads as W  # noqa: E402
 METRIC = "QSA layer decode tokens/s and prefill rows/s at 1 GB300; % of HBM / fp8 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 512 << 20
+DRAIN_BYTES = 256 << 20
+
+
+def flush_l2(flush, drain, i):
+    """Write a buffer larger than L2, then read another one larger than L2."""
+    flush.fill_(i & 0xFF)
+    return drain.sum()
 
 # DRAM bytes per launch of the sparse GQA kernel on the decode batch, from one
 # ncu capture (profiles/decode_batch_kernel_sections.md), keyed by a hash of
@@ -298,6 +307,7 @@ def run_ours(args):
     wl, cfg, gcfg, mv, packed, out, ws = build(spec, device)
     sargs = Q.step_args(wl.t, packed, out, mv)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    drain = torch.ones(DRAIN_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
 
     def step_direct():
@@ -336,7 +346,7 @@ def run_ours(args):
     barrier(dist, device)
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, drain, i)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -354,7 +364,7 @@ def run_ours(args):
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, drain, i)
         gev[i][0].record(stream)
         Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], packed, wl["token_to_req"],
                      wl["gate"], out, gws)
@@ -377,7 +387,7 @@ def run_ours(args):
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, drain, i)
         eev[i][0].record(stream)
         for k, v in host.items():
             wl.t[k].copy_(v, non_blocking=True)
@@ -411,7 +421,8 @@ def run_ours(args):
                                   f" r={spec.compress_ratio} topk={spec.token_topk}",
                        "gqa": f"{spec.hq}q/{spec.hkv}kv x128 bf16 page {spec.page}",
                        "parallelism": f"replicas x{world}",
-                       "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)"},
+                       "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, then a "
+                             f"{DRAIN_BYTES >> 20} MiB read to evict the written lines)"},
             "roofline": {"bound": "hbm", "kernel": "qsa sparse GQA (stage 4)",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm,

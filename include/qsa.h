@@ -149,7 +149,7 @@ qsa_status qsa_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx
  *               cblock_table[q, c / cpage], offset c % cpage
  *  logits       [rows, ld] fp32 (out); entries c >= V(p_i) are not written
  *  max_visible  upper bound of V(p) over the rows (ld >= max_visible)
- *  ws           scratch (row-group table), qsa_workspace_bytes() bytes
+ *  ws, ws_bytes unused by this build (may be NULL / 0)
  */
 qsa_status qsa_index_logits(const qsa_cfg* cfg, const void* q_idx,
                             const void* ccache, int32_t cpages,
@@ -281,9 +281,9 @@ size_t qsa_workspace_bytes(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg,
                            int32_t rows, int32_t reqs, int32_t max_visible);
 
 /* Number of kernel launches one qsa_layer_step call makes for these sizes:
- * 4 (compress with the logits row-group table, logits, top-k with the ring
- * commit, sparse GQA with its split merge), or 3 with skip_topk (compress,
- * ring commit, sparse GQA).  0 if invalid. */
+ * 4 (compress, logits, top-k with the ring commit, sparse GQA with its split
+ * merge), or 3 with skip_topk (compress, ring commit, sparse GQA).  0 if
+ * invalid.  All but the first use programmatic dependent launch. */
 int32_t qsa_step_launches(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t rows,
                           int32_t reqs, int32_t skip_topk);
 

@@ -122,11 +122,8 @@ int max_groups_for(int rows, int reqs, int R) {
 
 long long logits_ld(int max_visible) { return (static_cast<long long>(max_visible) + 3) / 4 * 4; }
 
-size_t logits_ws_bytes(int rows, int reqs, const qsa_cfg* c) {
-  int R, np;
-  logits_grouping(c, rows, reqs, &R, &np);
-  return align256(static_cast<size_t>(max_groups_for(rows, reqs, R)) * sizeof(int4)) + 256;
-}
+// The logits kernel needs no scratch (each CTA finds its own row group).
+size_t logits_ws_bytes(int, int, const qsa_cfg*) { return 0; }
 
 size_t gqa_ws_bytes(const qsa_gqa_cfg* g, int rows, int packed_width) {
   const int s = gqa_num_splits(rows, g->num_kv_heads, packed_width);
@@ -148,8 +145,8 @@ qsa_status do_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
                        const int32_t* token_to_req, const int32_t* query_start_loc,
                        const int32_t* logical_positions, void* ccache, int32_t cpages,
                        const int64_t* compressed_slots, int32_t rows, int32_t reqs,
-                       cudaStream_t stream, const LogitsParams* plan = nullptr,
-                       bool commit_ring = true, CompressParams* out_params = nullptr) {
+                       cudaStream_t stream, bool commit_ring = true,
+                       CompressParams* out_params = nullptr) {
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (rows < 0 || reqs < 0) return QSA_ERR_SHAPE;
@@ -202,9 +199,9 @@ qsa_status do_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
   if (out_params != nullptr) *out_params = p;
-  st = cuda_status(launch_compress(p, plan, stream));
+  st = cuda_status(launch_compress(p, stream, /*pdl=*/false));
   if (st != QSA_OK || !commit_ring) return st;
-  return cuda_status(launch_ring_commit(p, stream));
+  return cuda_status(launch_ring_commit(p, stream, /*pdl=*/true));
 }
 
 // Validates the logits arguments and fills the kernel parameters; the
@@ -214,19 +211,20 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
                          const int32_t* token_to_req, const int32_t* query_start_loc,
                          const int32_t* logical_positions, float* logits, int64_t ld,
                          int32_t max_visible, int32_t rows, int32_t reqs, void* ws,
-                         size_t ws_bytes, LogitsParams* out, int* npad_out, int* chunks_out) {
+                         size_t ws_bytes, LogitsParams* out, int* npad_out, int* chunks_out,
+                         int* groups_out) {
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (rows < 0 || reqs < 0 || max_visible < 0) return QSA_ERR_SHAPE;
   if (rows == 0 || max_visible == 0) return QSA_OK;
   if (reqs < 1 || cpages < 1 || cbt_stride < 1 || ld < max_visible) return QSA_ERR_SHAPE;
   if (!q_idx || !ccache || !cblock_table || !token_to_req || !query_start_loc ||
-      !logical_positions || !logits || !ws)
+      !logical_positions || !logits)
     return QSA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q_idx) | reinterpret_cast<uintptr_t>(ccache)) & 15)
     return QSA_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(ws) & 255) return QSA_ERR_WORKSPACE;
-  if (ws_bytes < logits_ws_bytes(rows, reqs, cfg)) return QSA_ERR_WORKSPACE;
+  (void)ws;
+  (void)ws_bytes;
 
   int R, npad;
   logits_grouping(cfg, rows, reqs, &R, &npad);
@@ -235,9 +233,6 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
   p.cblock_table = cblock_table;
   p.logical = logical_positions;
   p.qsl = query_start_loc;
-  p.groups = static_cast<int4*>(ws);
-  p.group_count = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) +
-                                         align256(static_cast<size_t>(max_groups) * sizeof(int4)));
   p.logits = logits;
   p.ccache = static_cast<const uint8_t*>(ccache);
   p.ld = ld;
@@ -246,11 +241,9 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
   p.cpage = cfg->cpage;
   p.reqs = reqs;
   p.rows_per_group = R;
-  p.max_groups = max_groups;
   p.n_heads = cfg->n_heads;
   p.ratio = cfg->compress_ratio;
   p.scale = 1.0f / (static_cast<float>(cfg->n_heads) * sqrtf(128.0f));
-  p.manual = cfg->cpage < 8 ? 1 : 0;
   p.row_bytes = 128 * elem_bytes(cfg);
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
@@ -261,30 +254,24 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
   long long tpc = (work + 4 * 152 - 1) / (4 * 152);
   if (tpc < 2) tpc = 2;
   if (tpc > max_tiles) tpc = max_tiles;
-  if (!p.manual && tpc * (128 / cfg->cpage) > 4096) tpc = 4096 / (128 / cfg->cpage);
+  if (tpc * (128 / cfg->cpage) > 4096) tpc = 4096 / (128 / cfg->cpage);
   p.tiles_per_cta = static_cast<int>(tpc);
   *chunks_out = static_cast<int>((max_tiles + tpc - 1) / tpc);
   *npad_out = npad;
+  *groups_out = max_groups;
   *out = p;
   return QSA_OK;
 }
 
 qsa_status launch_logits(const qsa_cfg* cfg, const LogitsParams& p, const void* q_idx,
-                         const void* ccache, int32_t rows, int32_t cpages, int npad, int chunks,
-                         bool plan_done, cudaStream_t stream) {
+                         int32_t rows, int npad, int chunks, int max_groups, bool pdl,
+                         cudaStream_t stream) {
   const int eb = elem_bytes(cfg);
-  CUtensorMap tq, tk;
+  CUtensorMap tq;
   if (!encode_rows_map(&tq, q_idx, eb, static_cast<long long>(rows) * cfg->n_heads, npad))
     return QSA_ERR_CUDA;
-  const int kbox = p.manual ? 8 : cfg->cpage;
-  if (!encode_rows_map(&tk, ccache, eb, static_cast<long long>(cpages) * cfg->cpage, kbox))
-    return QSA_ERR_CUDA;
-  if (!plan_done) {
-    qsa_status st = cuda_status(launch_logits_plan(p, stream));
-    if (st != QSA_OK) return st;
-  }
   return cuda_status(
-      launch_index_logits(p, tq, tk, cfg->index_dtype, npad, p.max_groups, chunks, stream));
+      launch_index_logits(p, tq, cfg->index_dtype, npad, max_groups, chunks, stream, pdl));
 }
 
 qsa_status do_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache, int32_t cpages,
@@ -293,17 +280,18 @@ qsa_status do_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache, 
                      float* logits, int64_t ld, int32_t max_visible, int32_t rows, int32_t reqs,
                      void* ws, size_t ws_bytes, cudaStream_t stream) {
   LogitsParams p{};
-  int npad = 0, chunks = 0;
+  int npad = 0, chunks = 0, groups = 0;
   qsa_status st = logits_params(cfg, q_idx, ccache, cpages, cblock_table, cbt_stride, token_to_req,
                                 query_start_loc, logical_positions, logits, ld, max_visible, rows,
-                                reqs, ws, ws_bytes, &p, &npad, &chunks);
+                                reqs, ws, ws_bytes, &p, &npad, &chunks, &groups);
   if (st != QSA_OK || rows == 0 || max_visible == 0) return st;
-  return launch_logits(cfg, p, q_idx, ccache, rows, cpages, npad, chunks, false, stream);
+  return launch_logits(cfg, p, q_idx, rows, npad, chunks, groups, /*pdl=*/false, stream);
 }
 
 qsa_status do_topk(const qsa_cfg* cfg, const float* logits, int64_t ld, int32_t max_visible,
                    const int32_t* logical_positions, int32_t* packed, int32_t rows,
-                   cudaStream_t stream, const CompressParams* ring = nullptr) {
+                   cudaStream_t stream, const CompressParams* ring = nullptr,
+                   unsigned* tickets = nullptr, int tickets_per_row = 0, bool pdl = false) {
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (rows < 0 || max_visible < 0) return QSA_ERR_SHAPE;
@@ -327,13 +315,16 @@ qsa_status do_topk(const qsa_cfg* cfg, const float* logits, int64_t ld, int32_t 
     p.do_ring = 1;
     p.ring = *ring;
   }
-  return cuda_status(launch_topk(p, stream));
+  p.tickets = tickets;
+  p.tickets_per_row = tickets_per_row;
+  return cuda_status(launch_topk(p, stream, pdl));
 }
 
 qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
                   const int32_t* block_table, int32_t bt_stride, const int32_t* packed,
                   int32_t packed_width, const int32_t* token_to_req, const void* gate, void* out,
-                  int32_t rows, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                  int32_t rows, void* ws, size_t ws_bytes, cudaStream_t stream,
+                  bool pdl = false, bool tickets_zeroed = false) {
   qsa_status st = check_gcfg(gcfg);
   if (st != QSA_OK) return st;
   if (rows < 0) return QSA_ERR_SHAPE;
@@ -370,7 +361,7 @@ qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
   }
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
-  return cuda_status(launch_sparse_gqa(p, stream));
+  return cuda_status(launch_sparse_gqa(p, stream, pdl, !tickets_zeroed));
 }
 
 // Layer-step workspace regions.
@@ -467,46 +458,57 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int pw = cfg->token_topk + cfg->compress_ratio;
+  const int splits = gqa_num_splits(a->rows, gcfg->num_kv_heads, pw);
+  // Kernels after the first start early (programmatic dependent launch) and
+  // wait on the device for their predecessor's results.
   if (skip_topk) {
-    // stage 1 only (ring commit included), then stage 4 on the given buffer
+    // stage 1 (ring commit included), then stage 4 on the given buffer
     st = do_compress(cfg, nullptr, nullptr, a->raw_keys, a->positions, a->cos_sin, a->q_norm_w,
                      a->k_norm_w, a->ring, a->ring_blocks, a->ring_pos, a->ring_block_table,
                      a->ring_bt_stride, a->token_to_req, a->query_start_loc, a->logical_positions,
                      a->ccache, a->cpages, a->compressed_slots, a->rows, a->reqs, s);
     if (st != QSA_OK) return st;
-  } else {
-    void* q_idx = w + L.q_idx;
-    float* logits = reinterpret_cast<float*>(w + L.logits);
-    LogitsParams lp{};
-    int npad = 0, chunks = 0;
-    const bool any_visible = a->max_visible > 0;
-    if (any_visible) {
-      st = logits_params(cfg, q_idx, a->ccache, a->cpages, a->cblock_table, a->cbt_stride,
-                         a->token_to_req, a->query_start_loc, a->logical_positions, logits, L.ld,
-                         a->max_visible, a->rows, a->reqs, w + L.logits_ws,
-                         L.gqa_ws - L.logits_ws, &lp, &npad, &chunks);
-      if (st != QSA_OK) return st;
-    }
-    // stage 1; the same launch builds the logits row-group table
-    CompressParams cp{};
-    st = do_compress(cfg, a->projected_q, q_idx, a->raw_keys, a->positions, a->cos_sin,
-                     a->q_norm_w, a->k_norm_w, a->ring, a->ring_blocks, a->ring_pos,
-                     a->ring_block_table, a->ring_bt_stride, a->token_to_req, a->query_start_loc,
-                     a->logical_positions, a->ccache, a->cpages, a->compressed_slots, a->rows,
-                     a->reqs, s, any_visible ? &lp : nullptr, /*commit_ring=*/false, &cp);
-    if (st != QSA_OK) return st;
-    if (any_visible) {
-      st = launch_logits(cfg, lp, q_idx, a->ccache, a->rows, a->cpages, npad, chunks,
-                         /*plan_done=*/true, s);
-      if (st != QSA_OK) return st;
-    }
-    // stage 3; the same launch commits the ring after every pooling read
-    st = do_topk(cfg, logits, L.ld, a->max_visible, a->logical_positions, a->packed, a->rows, s,
-                 &cp);
+    return do_gqa(gcfg, a->q, a->kv, a->block_table, a->bt_stride, a->packed, pw,
+                  a->token_to_req, a->gate, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s,
+                  /*pdl=*/true, /*tickets_zeroed=*/false);
+  }
+  void* q_idx = w + L.q_idx;
+  float* logits = reinterpret_cast<float*>(w + L.logits);
+  LogitsParams lp{};
+  int npad = 0, chunks = 0, groups = 0;
+  const bool any_visible = a->max_visible > 0;
+  if (any_visible) {
+    st = logits_params(cfg, q_idx, a->ccache, a->cpages, a->cblock_table, a->cbt_stride,
+                       a->token_to_req, a->query_start_loc, a->logical_positions, logits, L.ld,
+                       a->max_visible, a->rows, a->reqs, nullptr, 0, &lp, &npad, &chunks, &groups);
     if (st != QSA_OK) return st;
   }
+  // stage 1 (the ring commit waits for the top-k launch)
+  CompressParams cp{};
+  st = do_compress(cfg, a->projected_q, q_idx, a->raw_keys, a->positions, a->cos_sin,
+                   a->q_norm_w, a->k_norm_w, a->ring, a->ring_blocks, a->ring_pos,
+                   a->ring_block_table, a->ring_bt_stride, a->token_to_req, a->query_start_loc,
+                   a->logical_positions, a->ccache, a->cpages, a->compressed_slots, a->rows,
+                   a->reqs, s, /*commit_ring=*/false, &cp);
+  if (st != QSA_OK) return st;
+  if (any_visible) {
+    st = launch_logits(cfg, lp, q_idx, a->rows, npad, chunks, groups, /*pdl=*/true, s);
+    if (st != QSA_OK) return st;
+  }
+  // stage 3; the same launch commits the ring after every pooling read and
+  // clears the split-merge tickets of stage 4
+  unsigned* tickets = nullptr;
+  if (splits > 1) {
+    const size_t po = static_cast<size_t>(splits) * a->rows * gcfg->num_q_heads * 128 * sizeof(float);
+    const size_t pl = static_cast<size_t>(splits) * a->rows * gcfg->num_q_heads * sizeof(float);
+    tickets = reinterpret_cast<unsigned*>(w + L.gqa_ws + align256(po) + align256(pl));
+  }
+  st = do_topk(cfg, logits, L.ld, a->max_visible, a->logical_positions, a->packed, a->rows, s, &cp,
+               tickets, tickets ? gcfg->num_kv_heads : 0, /*pdl=*/any_visible);
+  if (st != QSA_OK) return st;
   return do_gqa(gcfg, a->q, a->kv, a->block_table, a->bt_stride, a->packed, pw, a->token_to_req,
-                a->gate, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s);
+                a->gate, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s, /*pdl=*/true,
+                /*tickets_zeroed=*/tickets != nullptr);
 }
 
 size_t qsa_workspace_bytes(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t rows,

@@ -14,10 +14,10 @@
 // row i: 8 half-warps, each owning n_heads / 8 head vectors, each lane 8
 // consecutive dims (one 16-byte load per head, all issued before any math);
 // RoPE partners (i, i + 32) sit 4 lanes apart.  CTA rows + i pools the group
-// completed by row i, if any, in parallel with the query CTAs.  An optional
-// last CTA builds the logits kernel's row-group table.
+// completed by row i, if any, in parallel with the query CTAs.
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
+#include "qsa_launch.cuh"
 #include "stage_helpers.cuh"
 
 namespace qsa {
@@ -115,13 +115,10 @@ __device__ __forceinline__ void store8(void* base, long long elem_off, const flo
 }
 
 template <int IDT>
-__global__ void __launch_bounds__(128) compress_kernel(const CompressParams P, const LogitsParams L,
-                                                       int do_plan) {
+__global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int b = blockIdx.x;
-  if (b >= 2 * P.rows) {  // the logits kernel's row-group table
-    if (do_plan) plan_groups(L);
-    return;
-  }
   const bool pool = b >= P.rows;
   const int row = pool ? b - P.rows : b;
   const int hw = threadIdx.x >> 4;       // half-warp 0..7
@@ -220,30 +217,24 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P, c
 // only if no later row of its request maps to the same slot, which gives the
 // sequential "later rows overwrite earlier rows" result without races.
 __global__ void __launch_bounds__(128) ring_commit_kernel(const CompressParams P) {
+  griddep_launch_dependents();
+  griddep_wait();  // every pooling read of the compress kernel is done
   const int row = blockIdx.x * 8 + (threadIdx.x >> 4);
   if (row < P.rows) ring_commit_row(P, row, threadIdx.x & 15);
 }
 
 }  // namespace
 
-cudaError_t launch_compress(const CompressParams& p, const LogitsParams* plan,
-                            cudaStream_t stream) {
+cudaError_t launch_compress(const CompressParams& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
-  LogitsParams L{};
-  if (plan != nullptr) L = *plan;
-  const int grid = 2 * p.rows + (plan != nullptr ? 1 : 0);
-  const int do_plan = plan != nullptr ? 1 : 0;
   if (p.index_dtype == 1)
-    compress_kernel<1><<<grid, 128, 0, stream>>>(p, L, do_plan);
-  else
-    compress_kernel<0><<<grid, 128, 0, stream>>>(p, L, do_plan);
-  return cudaGetLastError();
+    return launch_kernel(compress_kernel<1>, dim3(2 * p.rows), dim3(128), 0, stream, pdl, p);
+  return launch_kernel(compress_kernel<0>, dim3(2 * p.rows), dim3(128), 0, stream, pdl, p);
 }
 
-cudaError_t launch_ring_commit(const CompressParams& p, cudaStream_t stream) {
+cudaError_t launch_ring_commit(const CompressParams& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
-  ring_commit_kernel<<<(p.rows + 7) / 8, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(ring_commit_kernel, dim3((p.rows + 7) / 8), dim3(128), 0, stream, pdl, p);
 }
 
 }  // namespace qsa

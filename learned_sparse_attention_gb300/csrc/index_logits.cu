@@ -10,16 +10,22 @@
 // compressed keys are the M = 128 operand (A) and a group of rows of one
 // request, all their heads, is the N operand (B), kept in shared memory for
 // the whole CTA.  Per CTA:
-//   warp 0      producer: TMA loads of the B tile once, then of 128-key A
-//               tiles, one box per compressed page (pages are scattered, the
-//               block table gives their physical index), into a 4-stage ring;
-//   warp 1      allocates TMEM and issues tcgen05.mma (one thread), two
-//               accumulator buffers so the epilogue overlaps the next tile;
-//   warps 2..   epilogue: tcgen05.ld of the 128 x N accumulator, ReLU and
-//               head-sum per row, scale, coalesced fp32 stores.
+//   warp 0      allocates TMEM, loads the B tile with one TMA box and issues
+//               tcgen05.mma (one thread) into two accumulator buffers so the
+//               epilogue overlaps the next tile;
+//   warps 1-4   A-tile producers: thread m copies key row m of each 128-key
+//               tile with 16-byte cp.async straight into the 128-byte
+//               swizzled K-major layout, through a 4-stage ring.  The keys of
+//               a tile sit on 128 / cpage scattered compressed pages (2 KB
+//               each for e4m3 and 16-key pages); one TMA box per page was
+//               measured to cap a CTA at ~1 tile per 0.9 us, so the gather
+//               uses cp.async and TMA keeps the one large box (B);
+//   warps 5..   epilogue: one wide tcgen05.ld of the accumulator, branch-free
+//               ReLU / head sums, scale, coalesced fp32 stores.
 // Every wait is bounded (see mbar_wait); a timeout sets the error word.
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
+#include "qsa_launch.cuh"
 #include "stage_helpers.cuh"
 
 namespace qsa {
@@ -33,24 +39,26 @@ struct LogitsCfg {
   static constexpr int B_ATOM = NPAD * 128;
   static constexpr int B_BYTES = B_ATOM * ATOMS;
   static constexpr int STAGES = 4;
-  static constexpr int EPI_WG = NPAD == 256 ? 2 : 1;
-  static constexpr int THREADS = 64 + 128 * EPI_WG;
+  // two epilogue warpgroups (two warps per scheduler) once N >= 128: the
+  // ReLU + head sum costs about as many issue slots as the MMA takes
+  static constexpr int EPI_WG = NPAD >= 128 ? 2 : 1;
+  static constexpr int PRODUCERS = 128;                 // one thread per key row
+  static constexpr int THREADS = 32 + PRODUCERS + 128 * EPI_WG;
   static constexpr int KSTEPS = IDT == 1 ? 4 : 8;       // 32 bytes of K per MMA
   static constexpr uint32_t TMEM_COLS = 2 * NPAD;
   static constexpr int MAX_PAGES = 4096;                // page ids staged per CTA
   static constexpr int SMEM = 1024 + STAGES * A_STAGE + B_BYTES + 256 + MAX_PAGES * 4 + 32 * 4;
 };
 
-__global__ void __launch_bounds__(1024) logits_plan_kernel(const LogitsParams P) { plan_groups(P); }
-
 template <int IDT, int NPAD>
 __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
-    index_logits_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                        const __grid_constant__ CUtensorMap tmap_k, const LogitsParams P) {
+    index_logits_kernel(const __grid_constant__ CUtensorMap tmap_q, const LogitsParams P) {
   using C = LogitsCfg<IDT, NPAD>;
-  const int g = blockIdx.x;
-  if (g >= *P.group_count) return;
-  const int4 grp = P.groups[g];
+  griddep_launch_dependents();
+  // Everything up to griddep_wait reads only caller inputs (metadata, page
+  // tables), so it overlaps the tail of the compress kernel.
+  const int4 grp = find_group(P.qsl, P.reqs, P.rows_per_group, blockIdx.x, P.err);
+  if (grp.x < 0) return;
   const int row0 = grp.x, nrows = grp.y, req = grp.z;
   const int p_last = P.logical[row0 + nrows - 1];
   const int vmax = p_last < 0 ? 0 : (p_last + 1) / P.ratio;
@@ -77,16 +85,20 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   const int cpage = P.cpage;
   const int32_t* bt_row = P.cblock_table + static_cast<long long>(req) * P.cbt_stride;
   // Prologue: the group's visible-block counts and the physical compressed
-  // pages of this CTA's key range, resolved in parallel before any copy.
-  const int ppt = P.manual ? 0 : 128 / cpage;  // pages per 128-key tile
+  // pages of this CTA's key range (-1: beyond the table), resolved in parallel.
+  const int ppt = 128 / cpage;  // pages per 128-key tile
   const int page0 = t_begin * ppt;
   const int npages = min(ntiles * ppt, C::MAX_PAGES);
-  const int last_page = min((vmax - 1) / cpage, P.cbt_stride - 1);
+  const int last_page = (vmax - 1) / cpage;
   for (int i = threadIdx.x; i < npages; i += blockDim.x) {
-    int phys = bt_row[min(page0 + i, last_page)];
-    if (phys < 0 || phys >= P.cpages) {
-      flag_error(P.err);
-      phys = 0;
+    const int lp = page0 + i;
+    int phys = -1;
+    if (lp <= last_page && lp < P.cbt_stride) {
+      phys = bt_row[lp];
+      if (phys < 0 || phys >= P.cpages) {
+        flag_error(P.err);
+        phys = -1;
+      }
     }
     s_page[i] = phys;
   }
@@ -96,7 +108,7 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], C::PRODUCERS);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -106,7 +118,7 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
     mbar_init(bar_q, 1);
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == 0) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -115,64 +127,16 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   unsigned long long* err = P.err;
+  griddep_wait();  // the query tile and this step's compressed keys are written
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------ B tile + MMA issuer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
-      tma_prefetch_desc(&tmap_k);
       mbar_arrive_expect_tx(bar_q, C::B_BYTES);
 #pragma unroll
       for (int atom = 0; atom < C::ATOMS; ++atom)
         tma_load_2d(sB + atom * C::B_ATOM, &tmap_q, atom * 64, row0 * P.n_heads, bar_q);
-    }
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i % C::STAGES;
-      const uint32_t ph = (i / C::STAGES) & 1;
-      if (!mbar_wait(&empty[s], ph ^ 1, err)) break;
-      const int tile = t_begin + i;
-      uint8_t* dst = sA + s * C::A_STAGE;
-      if (!P.manual) {
-        const int pages = 128 / cpage;
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], C::A_STAGE);
-        __syncwarp();
-        for (int pg = lane; pg < pages; pg += 32) {
-          const int phys = s_page[min(i * pages + pg, npages - 1)];
-#pragma unroll
-          for (int atom = 0; atom < C::ATOMS; ++atom)
-            tma_load_2d(dst + atom * C::A_ATOM + pg * cpage * 128, &tmap_k, atom * 64,
-                        phys * cpage, &full[s]);
-        }
-      } else {
-        // Copy path for pages shorter than one 8-row swizzle group: plain
-        // 16-byte loads written in the same 128-byte swizzled layout.
-        constexpr int CHUNKS = 8 * C::ATOMS;
-        for (int idx = lane; idx < 128 * CHUNKS; idx += 32) {
-          const int m = idx / CHUNKS, c = idx % CHUNKS;
-          const int atom = c >> 3, cc = c & 7;
-          const int key = tile * 128 + m;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (key < vmax && key / cpage < P.cbt_stride) {
-            const int phys = bt_row[key / cpage];
-            if (phys >= 0 && phys < P.cpages) {
-              const uint8_t* src = P.ccache +
-                                   (static_cast<long long>(phys) * cpage + key % cpage) * P.row_bytes +
-                                   c * 16;
-              v = *reinterpret_cast<const uint4*>(src);
-            } else if (cc == 0 && atom == 0) {
-              flag_error(err);
-            }
-          }
-          *reinterpret_cast<uint4*>(dst + atom * C::A_ATOM + m * 128 + ((cc ^ (m & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
       uint32_t n_eff = ((nrows * P.n_heads + 31) / 32) * 32;
       if (n_eff > NPAD) n_eff = NPAD;
       const uint32_t idesc = umma_idesc(IDT == 1 ? 0u : 1u, 128, n_eff);
@@ -203,9 +167,44 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (warp <= C::PRODUCERS / 32) {
+    // ------------------------------------------------------ A-tile producers
+    // Thread m copies key row m of every tile: 8 (e4m3) or 16 (bf16) 16-byte
+    // cp.async into the 128-byte-swizzled K-major layout the MMA reads.  A
+    // tile is announced (proxy fence + arrive) once LAG newer tiles are in
+    // flight, so LAG + 1 tiles stream at a time.
+    constexpr int LAG = C::STAGES - 2;
+    constexpr int CH = 8 * C::ATOMS;
+    const int m = threadIdx.x - 32;
+    int issued = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int s = i % C::STAGES;
+      const uint32_t ph = (i / C::STAGES) & 1;
+      if (!mbar_wait(&empty[s], ph ^ 1, err)) break;
+      const int key = (t_begin + i) * 128 + m;
+      const int phys = s_page[min(i * ppt + m / cpage, npages - 1)];
+      const bool ok = key < vmax && phys >= 0;
+      const uint8_t* src = P.ccache + (static_cast<long long>(ok ? phys : 0) * cpage + (m % cpage)) *
+                                          P.row_bytes;
+      uint8_t* dst = sA + s * C::A_STAGE + m * 128;
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+        cp_async16(dst + (c >> 3) * C::A_ATOM + (((c & 7) ^ (m & 7)) << 4), src + c * 16,
+                   ok ? 16u : 0u);
+      cp_async_commit();
+      ++issued;
+      if (i >= LAG) {
+        cp_async_wait<LAG>();
+        fence_proxy_async_smem();
+        mbar_arrive(&full[(i - LAG) % C::STAGES]);
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int i = max(0, issued - LAG); i < issued; ++i) mbar_arrive(&full[i % C::STAGES]);
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wg = (warp - 2) >> 2;
+    const int wg = (warp - 1 - C::PRODUCERS / 32) >> 2;
     const int lane_base = 32 * (warp & 3);
     const int m = lane_base + lane;
     const int cols = nrows * P.n_heads;
@@ -218,26 +217,31 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
       if (!mbar_wait(&acc_full[a], aph, err)) break;
       tc_fence_after_sync();
       const int key = (t_begin + i) * 128 + m;
-      // One wide TMEM read of the warpgroup's columns, then the accumulator
-      // goes straight back to the MMA warp; sums and stores follow.
-      float v[COLS];
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_base) << 16) + a * NPAD + col_begin;
-      if constexpr (COLS == 32) tmem_ld32(taddr, v);
-      else if constexpr (COLS == 64) tmem_ld64_wait(taddr, v);
-      else tmem_ld128_wait(taddr, v);
-      tc_fence_before_sync();
-      mbar_arrive_relaxed(&acc_empty[a]);
-      // ReLU sums of 8-column segments, then a pairwise tree up to n_heads
-      // columns per row (n_heads is 8, 16, 32 or 64): branch-free, compact.
+      // Wide TMEM reads (at most 64 columns each) of the warpgroup's columns
+      // into ReLU sums of 8-column segments; then the accumulator goes
+      // straight back to the MMA warp, and the head sums and stores follow.
+      // 416 threads (two epilogue warpgroups) leave 128 registers a thread
+      constexpr int LDW = C::EPI_WG == 2 ? 32 : (COLS < 64 ? COLS : 64);
       constexpr int NSEG = COLS / 8;
       float seg[NSEG];
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_base) << 16) + a * NPAD + col_begin;
 #pragma unroll
-      for (int q = 0; q < NSEG; ++q) {
-        float t = 0.f;
+      for (int h = 0; h < COLS / LDW; ++h) {
+        float v[LDW];
+        if constexpr (LDW == 32) tmem_ld32(taddr + h * LDW, v);
+        else tmem_ld64_wait(taddr + h * LDW, v);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t += fmaxf(v[q * 8 + e], 0.f);
-        seg[q] = t;
+        for (int q = 0; q < LDW / 8; ++q) {
+          float t = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t += fmaxf(v[q * 8 + e], 0.f);
+          seg[h * (LDW / 8) + q] = t;
+        }
       }
+      tc_fence_before_sync();
+      mbar_arrive_relaxed(&acc_empty[a]);
+      // pairwise tree up to n_heads columns per row (n_heads is 8, 16, 32
+      // or 64): branch-free, compact.
       if (P.n_heads >= 16) {
 #pragma unroll
         for (int q = 0; q < NSEG / 2; ++q) seg[q] = seg[2 * q] + seg[2 * q + 1];
@@ -264,47 +268,48 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 0) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
 template <int IDT, int NPAD>
-cudaError_t launch_one(const LogitsParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                       int max_groups, int chunks, cudaStream_t stream) {
+cudaError_t launch_one(const LogitsParams& p, const CUtensorMap& tq, int max_groups, int chunks,
+                       cudaStream_t stream, bool pdl) {
   using C = LogitsCfg<IDT, NPAD>;
   auto kern = index_logits_kernel<IDT, NPAD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
-  kern<<<dim3(max_groups, chunks), C::THREADS, C::SMEM, stream>>>(tq, tk, p);
-  return cudaGetLastError();
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  return launch_kernel(kern, dim3(max_groups, chunks), dim3(C::THREADS), C::SMEM, stream, pdl, tq,
+                       p);
 }
 
 }  // namespace
 
-cudaError_t launch_logits_plan(const LogitsParams& p, cudaStream_t stream) {
-  logits_plan_kernel<<<1, 1024, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_index_logits(const LogitsParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                                int index_dtype, int npad, int max_groups, int chunks,
-                                cudaStream_t stream) {
+cudaError_t launch_index_logits(const LogitsParams& p, const CUtensorMap& tq, int index_dtype,
+                                int npad, int max_groups, int chunks, cudaStream_t stream,
+                                bool pdl) {
   if (max_groups <= 0 || chunks <= 0) return cudaSuccess;
   if (index_dtype == 1) {
     switch (npad) {
-      case 32: return launch_one<1, 32>(p, tq, tk, max_groups, chunks, stream);
-      case 64: return launch_one<1, 64>(p, tq, tk, max_groups, chunks, stream);
-      case 128: return launch_one<1, 128>(p, tq, tk, max_groups, chunks, stream);
-      case 256: return launch_one<1, 256>(p, tq, tk, max_groups, chunks, stream);
+      case 32: return launch_one<1, 32>(p, tq, max_groups, chunks, stream, pdl);
+      case 64: return launch_one<1, 64>(p, tq, max_groups, chunks, stream, pdl);
+      case 128: return launch_one<1, 128>(p, tq, max_groups, chunks, stream, pdl);
+      case 256: return launch_one<1, 256>(p, tq, max_groups, chunks, stream, pdl);
     }
   } else {
     switch (npad) {
-      case 32: return launch_one<0, 32>(p, tq, tk, max_groups, chunks, stream);
-      case 64: return launch_one<0, 64>(p, tq, tk, max_groups, chunks, stream);
-      case 128: return launch_one<0, 128>(p, tq, tk, max_groups, chunks, stream);
-      case 256: return launch_one<0, 256>(p, tq, tk, max_groups, chunks, stream);
+      case 32: return launch_one<0, 32>(p, tq, max_groups, chunks, stream, pdl);
+      case 64: return launch_one<0, 64>(p, tq, max_groups, chunks, stream, pdl);
+      case 128: return launch_one<0, 128>(p, tq, max_groups, chunks, stream, pdl);
+      case 256: return launch_one<0, 256>(p, tq, max_groups, chunks, stream, pdl);
     }
   }
   return cudaErrorInvalidValue;

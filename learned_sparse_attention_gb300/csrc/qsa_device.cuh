@@ -88,6 +88,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while its predecessor runs; it must wait here
+// before touching anything the predecessor writes.  Without the launch
+// attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the dependent grid launch once every CTA of this grid has executed it
+// (or exited); the dependent still waits for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

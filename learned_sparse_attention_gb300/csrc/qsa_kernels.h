@@ -31,37 +31,32 @@ struct CompressParams {
   unsigned long long* err;
 };
 
-struct LogitsParams;
-
-// plan: when non-null, the same launch also builds the logits row-group table.
-cudaError_t launch_compress(const CompressParams& p, const LogitsParams* plan, cudaStream_t stream);
-cudaError_t launch_ring_commit(const CompressParams& p, cudaStream_t stream);
+// pdl: launch with programmatic dependent launch (the kernel waits for the
+// previous kernel on the stream before touching its results).
+cudaError_t launch_compress(const CompressParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_ring_commit(const CompressParams& p, cudaStream_t stream, bool pdl);
 
 struct LogitsParams {
   const int32_t* cblock_table;
   const int32_t* logical;
   const int32_t* qsl;
-  int4* groups;           // x row0, y nrows, z req
-  int* group_count;
   float* logits;
-  const uint8_t* ccache;  // read directly by the copy path (cpage not a multiple of 8)
+  const uint8_t* ccache;  // compressed-key cache, gathered row by row
   long long ld;
   int cbt_stride, cpages, cpage;
-  int reqs, rows_per_group, max_groups;
+  int reqs, rows_per_group;
   int n_heads, ratio;
   float scale;
   int tiles_per_cta;
-  int manual;
   int row_bytes;
   unsigned long long* err;
 };
 
-// Builds the row-group table: each request's rows in chunks of rows_per_group.
-cudaError_t launch_logits_plan(const LogitsParams& p, cudaStream_t stream);
-// npad: padded MMA N (32, 64, 128 or 256); grid = (max_groups, chunks).
-cudaError_t launch_index_logits(const LogitsParams& p, const CUtensorMap& tmap_q,
-                                const CUtensorMap& tmap_k, int index_dtype, int npad,
-                                int max_groups, int chunks, cudaStream_t stream);
+// npad: padded MMA N (32, 64, 128 or 256); grid = (max_groups, chunks), CTA
+// x handles row group x (each request's rows in chunks of rows_per_group).
+cudaError_t launch_index_logits(const LogitsParams& p, const CUtensorMap& tmap_q, int index_dtype,
+                                int npad, int max_groups, int chunks, cudaStream_t stream,
+                                bool pdl);
 
 struct TopkParams {
   const float* logits;
@@ -72,9 +67,11 @@ struct TopkParams {
   unsigned long long* err;
   int do_ring;            // also commit the step's raw keys to the ring
   CompressParams ring;
+  unsigned* tickets;      // [rows, tickets_per_row] split-merge tickets to zero, or null
+  int tickets_per_row;
 };
 size_t topk_smem_bytes(int max_visible, int block_topk);
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl);
 
 struct GqaParams {
   const uint16_t* q;       // [rows, Hq, 128]
@@ -92,6 +89,9 @@ struct GqaParams {
   unsigned long long* err;
 };
 int gqa_num_splits(int rows, int hkv, int packed_width);
-cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream);
+// zero_tickets: clear the merge tickets first (false when a preceding kernel
+// of the same step already did).
+cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
+                              bool zero_tickets = true);
 
 }  // namespace qsa

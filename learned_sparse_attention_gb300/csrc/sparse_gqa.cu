@@ -29,6 +29,7 @@
 // given.
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
+#include "qsa_launch.cuh"
 
 namespace qsa {
 namespace {
@@ -106,8 +107,19 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
   const int g = lane >> 2, t = lane & 3;
   const int Wcols = P.packed_width - 1;
 
+  griddep_launch_dependents();
   const int req = P.token_to_req[row];
   const int32_t* prow = P.packed + static_cast<long long>(row) * P.packed_width;
+  // Q^T fragments (B operand of S^T = K.Q^T): head kvh*8 + g, 2 dims per
+  // register; a caller input, loaded before waiting for the top-k kernel.
+  const uint16_t* qh = P.q + (static_cast<long long>(row) * P.hq + kvh * kG + g) * 128;
+  uint32_t qb[8][2];
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    qb[kk][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t);
+    qb[kk][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t);
+  }
+  griddep_wait();  // the packed selection (and merge tickets) are written
   int n = prow[Wcols];
   bool bad_row = req < 0;
   if (n < 0 || n > Wcols) {
@@ -130,14 +142,6 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     ntok = kMaxTok;
   }
 
-  // Q^T fragments (B operand of S^T = K.Q^T): head kvh*8 + g, 2 dims per register.
-  const uint16_t* qh = P.q + (static_cast<long long>(row) * P.hq + kvh * kG + g) * 128;
-  uint32_t qb[8][2];
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    qb[kk][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t);
-    qb[kk][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t);
-  }
 
   float o[8][4];
 #pragma unroll
@@ -318,6 +322,8 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
 
 // Log-sum-exp merge of the split partials, then bf16 rounding and the gate.
 __global__ void __launch_bounds__(256) gqa_merge_kernel(const GqaParams P) {
+  griddep_launch_dependents();
+  griddep_wait();  // all split partials are written
   const int row = blockIdx.x;
   for (int idx = threadIdx.x; idx < P.hq * 16; idx += blockDim.x) merge8(P, row, idx >> 4, (idx & 15) * 8);
 }
@@ -339,7 +345,8 @@ int gqa_num_splits(int rows, int hkv, int packed_width) {
   return static_cast<int>(s);
 }
 
-cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream) {
+cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
+                              bool zero_tickets) {
   if (p.rows == 0) return cudaSuccess;
   if (static_cast<long long>(p.num_blocks) * p.hkv * p.page >= static_cast<long long>(kBadRow))
     return cudaErrorInvalidValue;
@@ -351,15 +358,15 @@ cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  if (p.splits > 1 && p.counters != nullptr) {
+  if (p.splits > 1 && p.counters != nullptr && zero_tickets) {
     cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(unsigned) * p.rows * p.hkv, stream);
     if (e != cudaSuccess) return e;
+    pdl = false;  // a memset node sits between this kernel and its predecessor
   }
-  gqa_kernel<<<dim3(p.rows * p.hkv, p.splits), 128, kSmem, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(gqa_kernel, dim3(p.rows * p.hkv, p.splits), dim3(128), kSmem, stream,
+                                pdl, p);
   if (e != cudaSuccess || p.splits == 1 || p.counters != nullptr) return e;
-  gqa_merge_kernel<<<p.rows, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(gqa_merge_kernel, dim3(p.rows), dim3(256), 0, stream, true, p);
 }
 
 }  // namespace qsa

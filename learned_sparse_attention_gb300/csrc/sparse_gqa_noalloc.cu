@@ -111,7 +111,7 @@ extern "C" qsa_status qsa_sparse_gqa_noalloc(const qsa_gqa_cfg* gcfg, const void
   }
   p.err = qsa::internal_error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
-  return qsa::launch_sparse_gqa(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return qsa::launch_sparse_gqa(p, static_cast<cudaStream_t>(stream), /*pdl=*/false) == cudaSuccess
              ? QSA_OK
              : QSA_ERR_CUDA;
 }

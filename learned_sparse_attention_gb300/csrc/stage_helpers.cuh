@@ -1,7 +1,7 @@
 // Block-level pieces shared by several kernels of the layer step so that small
 // jobs ride along in a neighbouring launch instead of a launch of their own:
 // the ring commit (stage 1 bookkeeping, done by the top-k launch) and the
-// row-group table of the logits kernel (built by the compress launch).
+// row group of each logits CTA.
 #pragma once
 
 #include "qsa_device.cuh"
@@ -32,25 +32,29 @@ __device__ __forceinline__ void ring_commit_row(const CompressParams& P, int row
     P.ring_pos[ring_slot * 3 + lane16] = P.positions[static_cast<long long>(row) * 3 + lane16];
 }
 
-// Row-group table of the logits kernel: each request's rows in chunks of
-// rows_per_group, in request order.  Executed by one whole block (any size
-// that is a multiple of 32, at most 1024 threads).
-__device__ __forceinline__ void plan_groups(const LogitsParams& P) {
+// Row group g of the logits kernel, found by the whole block: the rows of
+// each request in chunks of R, numbered in request order.  Returns
+// (row0, nrows, request, 0), or row0 = -1 when g is past the last group.
+__device__ __forceinline__ int4 find_group(const int32_t* qsl, int reqs, int R, int g,
+                                           unsigned long long* err) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
+  __shared__ int4 found;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
-  if (tid == 0) carry = 0;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  if (tid == 0) {
+    carry = 0;
+    found = make_int4(-1, 0, 0, 0);
+  }
   __syncthreads();
-  const int R = P.rows_per_group;
-  for (int base = 0; base < P.reqs; base += blockDim.x) {
+  for (int base = 0; base < reqs; base += blockDim.x) {
     const int q = base + tid;
     int n = 0, start = 0;
-    if (q < P.reqs) {
-      start = P.qsl[q];
-      n = P.qsl[q + 1] - start;
+    if (q < reqs) {
+      start = qsl[q];
+      n = qsl[q + 1] - start;
       if (n < 0) {
-        flag_error(P.err);
+        if (g == 0) flag_error(err);
         n = 0;
       }
     }
@@ -74,19 +78,17 @@ __device__ __forceinline__ void plan_groups(const LogitsParams& P) {
     }
     __syncthreads();
     const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - ng;
-    for (int k = 0; k < ng; ++k) {
-      const int idx = excl + k;
-      if (idx >= P.max_groups) {
-        flag_error(P.err);
-        break;
-      }
-      P.groups[idx] = make_int4(start + k * R, min(R, n - k * R), q, 0);
+    if (q < reqs && g >= excl && g < excl + ng) {
+      const int k = g - excl;
+      found = make_int4(start + k * R, min(R, n - k * R), q, 0);
     }
     __syncthreads();
     if (tid == 0) carry += warp_tot[nwarps - 1];
+    const bool done = found.x >= 0;
     __syncthreads();
+    if (done) break;
   }
-  if (tid == 0) *P.group_count = min(carry, P.max_groups);
+  return found;
 }
 
 }  // namespace qsa

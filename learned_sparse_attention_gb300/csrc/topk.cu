@@ -17,6 +17,7 @@
 // visible block without reading logits.
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
+#include "qsa_launch.cuh"
 #include "stage_helpers.cuh"
 
 namespace qsa {
@@ -75,6 +76,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
   uint32_t* keys = sm;
   int* sel = reinterpret_cast<int*>(sm + P.max_visible);
 
+  griddep_launch_dependents();
+  if (P.tickets != nullptr && threadIdx.x < P.tickets_per_row)
+    P.tickets[static_cast<long long>(blockIdx.x) * P.tickets_per_row + threadIdx.x] = 0u;
+  griddep_wait();  // logits (and, transitively, the compress kernel) are done
   const int row = blockIdx.x, tid = threadIdx.x;
   const int r = P.ratio;
   const int kb = P.token_topk / r;
@@ -278,6 +283,10 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
   __shared__ uint32_t s_min[kRegWarps], s_max[kRegWarps];
   __shared__ int s_digit, s_k;
 
+  griddep_launch_dependents();
+  if (P.tickets != nullptr && threadIdx.x < P.tickets_per_row)
+    P.tickets[static_cast<long long>(blockIdx.x) * P.tickets_per_row + threadIdx.x] = 0u;
+  griddep_wait();  // logits (and, transitively, the compress kernel) are done
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = P.ratio;
   const int kb = P.token_topk / r;
@@ -448,18 +457,15 @@ size_t topk_smem_bytes(int max_visible, int block_topk) {
   return static_cast<size_t>(max_visible) * 4 + static_cast<size_t>(block_topk) * 4 + 16;
 }
 
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
-  if (p.max_visible <= kRegKeys * kRegThreads && p.token_topk / p.ratio <= kRegKeys * kRegThreads / 4) {
-    topk_reg_kernel<<<p.rows, kRegThreads, 0, stream>>>(p);
-    return cudaGetLastError();
-  }
+  if (p.max_visible <= kRegKeys * kRegThreads && p.token_topk / p.ratio <= kRegKeys * kRegThreads / 4)
+    return launch_kernel(topk_reg_kernel, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
   const size_t smem = topk_smem_bytes(p.max_visible, p.token_topk / p.ratio);
   cudaError_t e =
       cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  topk_kernel<<<p.rows, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(topk_kernel, dim3(p.rows), dim3(kThreads), smem, stream, pdl, p);
 }
 
 }  // namespace qsa

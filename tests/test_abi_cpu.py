@@ -106,11 +106,14 @@ def test_null_and_shape_errors(lib):
     g3 = Q.make_gqa_cfg(32, 4, 40, 10)
     assert lib.qsa_sparse_gqa(ctypes.byref(g3), d, d, d, 1, d, 68, d, None, d, 4, None, 0,
                               None) == 2
-    # logits: ld smaller than max_visible; workspace misaligned
+    # logits: ld smaller than max_visible; negative rows
     assert lib.qsa_index_logits(ctypes.byref(cfg), d, d, 1, d, 1, d, d, d, d, 100, 200, 4, 1, d,
                                 1 << 20, None) == 2
-    assert lib.qsa_index_logits(ctypes.byref(cfg), d, d, 1, d, 1, d, d, d, d, 256, 200, 4, 1,
-                                ctypes.c_void_p(300), 1 << 20, None) == 5
+    assert lib.qsa_index_logits(ctypes.byref(cfg), d, d, 1, d, 1, d, d, d, d, 256, 200, -1, 1,
+                                None, 0, None) == 2
+    # misaligned compressed cache
+    assert lib.qsa_index_logits(ctypes.byref(cfg), d, ctypes.c_void_p(264), 1, d, 1, d, d, d, d,
+                                256, 200, 4, 1, None, 0, None) == 1
     # top-k beyond the shared-memory limit of this build
     assert lib.qsa_topk(ctypes.byref(cfg), d, 1 << 20, 1 << 20, d, d, 4, None) == 4
 
