@@ -38,7 +38,8 @@ struct LogitsCfg {
   static constexpr int A_STAGE = A_ATOM * ATOMS;
   static constexpr int B_ATOM = NPAD * 128;
   static constexpr int B_BYTES = B_ATOM * ATOMS;
-  static constexpr int STAGES = 4;
+  // decode-sized tiles (N <= 64) keep 3 stages so that 4 CTAs fit on an SM
+  static constexpr int STAGES = NPAD <= 64 ? 3 : 4;
   // two epilogue warpgroups (two warps per scheduler) once N >= 128: the
   // ReLU + head sum costs about as many issue slots as the MMA takes
   static constexpr int EPI_WG = NPAD >= 128 ? 2 : 1;
@@ -46,8 +47,9 @@ struct LogitsCfg {
   static constexpr int THREADS = 32 + PRODUCERS + 128 * EPI_WG;
   static constexpr int KSTEPS = IDT == 1 ? 4 : 8;       // 32 bytes of K per MMA
   static constexpr uint32_t TMEM_COLS = 2 * NPAD;
-  static constexpr int MAX_PAGES = 4096;                // page ids staged per CTA
-  static constexpr int SMEM = 1024 + STAGES * A_STAGE + B_BYTES + 256 + MAX_PAGES * 4 + 32 * 4;
+  static constexpr int MAX_PAGES = 4096;                // page ids staged per CTA (at most)
+  // shared memory without the page-id array, which is sized per launch
+  static constexpr int SMEM_BASE = 1024 + STAGES * A_STAGE + B_BYTES + 256 + 32 * 4;
 };
 
 template <int IDT, int NPAD>
@@ -78,8 +80,8 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* bar_q = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 1);
-  int* s_page = reinterpret_cast<int*>(smem_raw + pad + C::STAGES * C::A_STAGE + C::B_BYTES + 256);
-  int* s_vis = s_page + C::MAX_PAGES;  // visible blocks of the group's rows
+  int* s_vis = reinterpret_cast<int*>(smem_raw + pad + C::STAGES * C::A_STAGE + C::B_BYTES + 256);
+  int* s_page = s_vis + 32;  // tiles_per_cta * (128 / cpage) entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cpage = P.cpage;
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   // pages of this CTA's key range (-1: beyond the table), resolved in parallel.
   const int ppt = 128 / cpage;  // pages per 128-key tile
   const int page0 = t_begin * ppt;
-  const int npages = min(ntiles * ppt, C::MAX_PAGES);
+  const int npages = ntiles * ppt;  // <= tiles_per_cta * ppt <= MAX_PAGES (host)
   const int last_page = (vmax - 1) / cpage;
   for (int i = threadIdx.x; i < npages; i += blockDim.x) {
     const int lp = page0 + i;
@@ -279,16 +281,17 @@ cudaError_t launch_one(const LogitsParams& p, const CUtensorMap& tq, int max_gro
                        cudaStream_t stream, bool pdl) {
   using C = LogitsCfg<IDT, NPAD>;
   auto kern = index_logits_kernel<IDT, NPAD>;
+  const int smem = C::SMEM_BASE + p.tiles_per_cta * (128 / p.cpage) * 4;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BASE + C::MAX_PAGES * 4);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  return launch_kernel(kern, dim3(max_groups, chunks), dim3(C::THREADS), C::SMEM, stream, pdl, tq,
-                       p);
+  return launch_kernel(kern, dim3(max_groups, chunks), dim3(C::THREADS), smem, stream, pdl, tq, p);
 }
 
 }  // namespace
