@@ -239,6 +239,7 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
   p.cbt_stride = cbt_stride;
   p.cpages = cpages;
   p.cpage = cfg->cpage;
+  p.rows = rows;
   p.reqs = reqs;
   p.rows_per_group = R;
   p.n_heads = cfg->n_heads;

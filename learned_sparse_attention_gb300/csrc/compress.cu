@@ -167,12 +167,18 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
   if (slot < 0 || (threadIdx.x >> 5) != 0) return;
   const int r = P.ratio;
   const int first_row = P.qsl[req];
+  if (first_row < 0 || first_row > row) {  // inconsistent query_start_loc
+    if (threadIdx.x == 0) flag_error(P.err);
+    return;
+  }
   const int step_start = P.logical[first_row];
   const int ring_block = P.ring_bt[static_cast<long long>(req) * P.ring_bt_stride];
   const long long nslots = static_cast<long long>(P.cpages) * P.cpage;
   const int t0 = p - r + 1;
   const bool ring_needed = t0 < step_start;
-  if (slot >= nslots || t0 < 0 ||
+  // raw keys of this step are rows first_row .. first_row + (p - step_start),
+  // which must not pass this row
+  if (slot >= nslots || t0 < 0 || p - step_start > row - first_row ||
       (ring_needed && (ring_block < 0 || ring_block >= P.ring_blocks))) {
     if (threadIdx.x == 0) flag_error(P.err);
     return;

@@ -38,18 +38,25 @@ struct LogitsCfg {
   static constexpr int A_STAGE = A_ATOM * ATOMS;
   static constexpr int B_ATOM = NPAD * 128;
   static constexpr int B_BYTES = B_ATOM * ATOMS;
-  // decode-sized tiles (N <= 64) keep 3 stages so that 4 CTAs fit on an SM
-  static constexpr int STAGES = NPAD <= 64 ? 3 : 4;
-  // two epilogue warpgroups (two warps per scheduler) once N >= 128: the
-  // ReLU + head sum costs about as many issue slots as the MMA takes
-  static constexpr int EPI_WG = NPAD >= 128 ? 2 : 1;
+  static constexpr int MAX_PAGES = 4096;                // page ids staged per CTA (at most)
+  // decode-sized tiles (N <= 64) keep 3 stages so that 4 CTAs fit on an SM;
+  // from N = 128 on a CTA has the SM to itself (TMEM, registers), and the A
+  // ring takes what shared memory is left after B and the page ids (at most
+  // 8 stages): the A tiles come from L2 and need many bytes in flight.
+  static constexpr int SMEM_LIMIT = 226 * 1024;  // 227 KB per CTA, less static smem
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - B_BYTES - 256 - 128 - MAX_PAGES * 4) / A_STAGE;
+  static constexpr int STAGES = NPAD <= 64 ? 3 : (STAGES_FIT < 8 ? STAGES_FIT : 8);
+  // from N = 128 on one epilogue warpgroup per 64 accumulator columns: the
+  // ReLU + head sums are chains of dependent adds, and only several warps
+  // per scheduler hide their latency behind the MMA of the next tile
+  static constexpr int EPI_WG = NPAD >= 128 ? NPAD / 64 : 1;
   static constexpr int PRODUCERS = 128;                 // one thread per key row
   static constexpr int THREADS = 32 + PRODUCERS + 128 * EPI_WG;
   static constexpr int KSTEPS = IDT == 1 ? 4 : 8;       // 32 bytes of K per MMA
   static constexpr uint32_t TMEM_COLS = 2 * NPAD;
-  static constexpr int MAX_PAGES = 4096;                // page ids staged per CTA (at most)
   // shared memory without the page-id array, which is sized per launch
   static constexpr int SMEM_BASE = 1024 + STAGES * A_STAGE + B_BYTES + 256 + 32 * 4;
+  static_assert(STAGES >= 3 && SMEM_BASE + MAX_PAGES * 4 <= SMEM_LIMIT, "shared memory");
 };
 
 template <int IDT, int NPAD>
@@ -59,7 +66,7 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   griddep_launch_dependents();
   // Everything up to griddep_wait reads only caller inputs (metadata, page
   // tables), so it overlaps the tail of the compress kernel.
-  const int4 grp = find_group(P.qsl, P.reqs, P.rows_per_group, blockIdx.x, P.err);
+  const int4 grp = find_group(P.qsl, P.reqs, P.rows, P.rows_per_group, blockIdx.x, P.err);
   if (grp.x < 0) return;
   const int row0 = grp.x, nrows = grp.y, req = grp.z;
   const int p_last = P.logical[row0 + nrows - 1];
@@ -219,26 +226,37 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
       if (!mbar_wait(&acc_full[a], aph, err)) break;
       tc_fence_after_sync();
       const int key = (t_begin + i) * 128 + m;
-      // Wide TMEM reads (at most 64 columns each) of the warpgroup's columns
-      // into ReLU sums of 8-column segments; then the accumulator goes
-      // straight back to the MMA warp, and the head sums and stores follow.
-      // 416 threads (two epilogue warpgroups) leave 128 registers a thread
-      constexpr int LDW = C::EPI_WG == 2 ? 32 : (COLS < 64 ? COLS : 64);
+      // The warpgroup's columns in 32-column TMEM reads, double-buffered so
+      // that the next read is in flight while the current one is summed.  An
+      // 8-column segment is relu-summed with max(x, 0) on five columns (ALU
+      // pipe) and (x + |x|) / 2 on three (FMA pipe), which keeps the two
+      // pipes about equally loaded; then the accumulator goes straight back
+      // to the MMA warp, and the head sums and stores follow.
+      constexpr int NCH = COLS / 32;
       constexpr int NSEG = COLS / 8;
       float seg[NSEG];
+      uint32_t buf[2][32];
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_base) << 16) + a * NPAD + col_begin;
+      tmem_ld32_issue(taddr, buf[0]);
+      tmem_wait_ld32(buf[0]);
 #pragma unroll
-      for (int h = 0; h < COLS / LDW; ++h) {
-        float v[LDW];
-        if constexpr (LDW == 32) tmem_ld32(taddr + h * LDW, v);
-        else tmem_ld64_wait(taddr + h * LDW, v);
+      for (int h = 0; h < NCH; ++h) {
+        if (h + 1 < NCH) tmem_ld32_issue(taddr + (h + 1) * 32, buf[(h + 1) & 1]);
 #pragma unroll
-        for (int q = 0; q < LDW / 8; ++q) {
-          float t = 0.f;
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t* x = &buf[h & 1][q * 8];
+          float t = 0.f, u = 0.f, w = 0.f;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) t += fmaxf(v[q * 8 + e], 0.f);
-          seg[h * (LDW / 8) + q] = t;
+          for (int e = 0; e < 5; ++e) t += fmaxf(__uint_as_float(x[e]), 0.f);
+#pragma unroll
+          for (int e = 5; e < 8; ++e) {
+            const float f = __uint_as_float(x[e]);
+            u += f;
+            w += fabsf(f);
+          }
+          seg[h * 4 + q] = fmaf(0.5f, u + w, t);
         }
+        if (h + 1 < NCH) tmem_wait_ld32(buf[(h + 1) & 1]);
       }
       tc_fence_before_sync();
       mbar_arrive_relaxed(&acc_empty[a]);
@@ -288,6 +306,10 @@ cudaError_t launch_one(const LogitsParams& p, const CUtensorMap& tq, int max_gro
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BASE + C::MAX_PAGES * 4);
+    if (e != cudaSuccess) return e;
+    // all of the unified L1 / shared memory as shared memory, so that as many
+    // CTAs as the shared-memory footprint allows are resident on an SM
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }

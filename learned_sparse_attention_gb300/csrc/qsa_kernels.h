@@ -44,7 +44,7 @@ struct LogitsParams {
   const uint8_t* ccache;  // compressed-key cache, gathered row by row
   long long ld;
   int cbt_stride, cpages, cpage;
-  int reqs, rows_per_group;
+  int rows, reqs, rows_per_group;
   int n_heads, ratio;
   float scale;
   int tiles_per_cta;

@@ -356,6 +356,8 @@ cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gqa_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   if (p.splits > 1 && p.counters != nullptr && zero_tickets) {

@@ -16,8 +16,13 @@ namespace qsa {
 __device__ __forceinline__ void ring_commit_row(const CompressParams& P, int row, int lane16) {
   const int req = P.token_to_req[row];
   if (req < 0 || req >= P.reqs) return;  // counted by the compress kernel
+  const int last_row = P.qsl[req + 1] - 1;
+  if (last_row < row || last_row >= P.rows) {  // inconsistent query_start_loc
+    if (lane16 == 0) flag_error(P.err);
+    return;
+  }
   const int p = P.logical[row];
-  const int p_last = P.logical[P.qsl[req + 1] - 1];
+  const int p_last = P.logical[last_row];
   if (p + P.S <= p_last) return;  // overwritten later in this step
   const int ring_block = P.ring_bt[static_cast<long long>(req) * P.ring_bt_stride];
   if (ring_block < 0 || ring_block >= P.ring_blocks || p < 0) {
@@ -35,7 +40,7 @@ __device__ __forceinline__ void ring_commit_row(const CompressParams& P, int row
 // Row group g of the logits kernel, found by the whole block: the rows of
 // each request in chunks of R, numbered in request order.  Returns
 // (row0, nrows, request, 0), or row0 = -1 when g is past the last group.
-__device__ __forceinline__ int4 find_group(const int32_t* qsl, int reqs, int R, int g,
+__device__ __forceinline__ int4 find_group(const int32_t* qsl, int reqs, int rows, int R, int g,
                                            unsigned long long* err) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
@@ -53,7 +58,7 @@ __device__ __forceinline__ int4 find_group(const int32_t* qsl, int reqs, int R, 
     if (q < reqs) {
       start = qsl[q];
       n = qsl[q + 1] - start;
-      if (n < 0) {
+      if (n < 0 || start < 0 || start + n > rows) {  // rows outside [0, rows): skipped
         if (g == 0) flag_error(err);
         n = 0;
       }

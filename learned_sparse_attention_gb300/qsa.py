@@ -249,6 +249,9 @@ def step_args(t: dict, packed, out, max_visible) -> QsaStepArgs:
     a.bt_stride = t["block_table"].shape[1]
     a.gate = _ptr(t.get("gate"), torch.bfloat16)
     a.out = _ptr(out, torch.bfloat16)
+    # the struct holds raw device addresses: keep the tensors behind them alive
+    # for as long as the struct is
+    a._tensors = (dict(t), packed, out)
     return a
 
 
