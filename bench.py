@@ -49,9 +49,9 @@ def flush_l2(flush, drain, i):
     return drain.sum()
 
 # DRAM bytes per launch of the sparse GQA kernel on the decode batch, from one
-# ncu capture (profiles/decode_batch_kernel_sections.md), keyed by a hash of
+# ncu capture (the decode-batch kernel-sections summary), keyed by a hash of
 # the kernel sources it was taken on; any other source reports null.
-GQA_TRAFFIC = {"401eff568cd728b4": 270356736 + 3680768}
+GQA_TRAFFIC = {"39209aefb738629f": 270382592 + 3614720}
 GQA_SOURCES = ("learned_sparse_attention_gb300/csrc/sparse_gqa.cu",
                "learned_sparse_attention_gb300/csrc/qsa_device.cuh")
 
@@ -297,6 +297,61 @@ def run_reference(args):
     return 0
 
 
+def prefill_report(device, steps, flush, drain):
+    """The chunked-prefill workload (one request, 16384 new rows after a
+    32768-token prefix): layer-step rows/s, and the index-logits kernel alone
+    against the fp8 tensor peak (FLOPs = visible keys x heads x 128 x 2)."""
+    spec = W.named_spec("chunked_prefill")
+    wl, cfg, gcfg, mv, packed, out, ws = build(spec, device)
+    sargs = Q.step_args(wl.t, packed, out, mv)
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        Q.layer_step(cfg, gcfg, sargs, ws)
+    torch.cuda.synchronize()
+
+    def timed(fn):
+        ts = []
+        for i in range(steps):
+            flush_l2(flush, drain, i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    step_ms = timed(lambda: Q.layer_step(cfg, gcfg, sargs, ws))
+    t = wl.t
+    q_idx = torch.empty((spec.rows, spec.n_heads, 128),
+                        dtype=torch.uint8 if spec.index_dtype == W.DTYPE_E4M3 else torch.bfloat16,
+                        device=device)
+    Q.compress(cfg, t["projected_q"], q_idx, t["raw_keys"], t["positions"], t["cos_sin"],
+               t["q_norm_w"], t["k_norm_w"], t["ring"], t.get("ring_pos"), t["ring_block_table"],
+               t["token_to_req"], t["query_start_loc"], t["logical_positions"], t["ccache"],
+               t["compressed_slots"])
+    logits = torch.empty((spec.rows, (mv + 3) // 4 * 4), dtype=torch.float32, device=device)
+    lws = torch.empty(256, dtype=torch.uint8, device=device)
+    logits_ms = timed(lambda: Q.index_logits(cfg, q_idx, t["ccache"], t["cblock_table"],
+                                             t["token_to_req"], t["query_start_loc"],
+                                             t["logical_positions"], logits, mv, lws))
+    if Q.check_errors() != 0:
+        raise RuntimeError("device error word set during the prefill measurement")
+    vis = ((t["logical_positions"].long() + 1) // spec.compress_ratio).clamp(min=0)
+    flops = float(vis.sum()) * spec.n_heads * 128 * 2
+    peaks, peak_kind = load_peaks()
+    fp8 = 2.0 * float(peaks["bf16_tflops"])
+    tf = flops / (logits_ms / 1000.0) / 1e12
+    res = {"workload": spec.name, "rows": spec.rows, "steps": steps,
+           "ms_per_step": step_ms, "value": spec.rows / (step_ms / 1000.0), "unit": "prefill rows/s",
+           "index_logits": {"bound": "tensor", "achieved": tf, "peak": fp8, "unit": "TFLOP/s",
+                            "frac": tf / fp8, "kernel_ms": logits_ms, "flops_per_launch": flops,
+                            "peak_source": f"2 x {peak_kind} bf16_tflops (nominal fp8/bf16 ratio)"}}
+    del wl, packed, out, ws, logits, q_idx
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     dist = init_dist(world, local, "nccl")
@@ -401,6 +456,9 @@ def run_ours(args):
         raise RuntimeError("device error word set during the timed steps")
 
     launches_per_step = Q.step_launches(cfg, gcfg, spec.rows, spec.reqs)
+    prefill = None
+    if rank == 0 and world == 1 and spec.name == "decode_batch" and not args.no_prefill:
+        prefill = prefill_report(device, 3, flush, drain)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -440,6 +498,7 @@ def run_ours(args):
             "gpu_launches": launches_per_step * args.steps,
             "launch": "CUDA graph of one qsa_layer_step call (value); direct calls (e2e)",
             "clocks": clk,
+            "prefill": prefill,
         }
         print(json.dumps(line))
     if dist is not None:
@@ -455,6 +514,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_batch", choices=list(W.NAMED))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the chunked-prefill rows/s and index-logits measurement")
     ap.add_argument("--ref-budget", type=float, default=15.0)
     args = ap.parse_args()
     if args.impl == "reference":

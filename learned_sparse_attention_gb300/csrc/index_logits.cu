@@ -67,14 +67,24 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   // Everything up to griddep_wait reads only caller inputs (metadata, page
   // tables), so it overlaps the tail of the compress kernel.
   const int4 grp = find_group(P.qsl, P.reqs, P.rows, P.rows_per_group, blockIdx.x, P.err);
-  if (grp.x < 0) return;
+  // The kernels after this one rely on "logits complete" implying "compress
+  // complete", so CTA (0, 0) waits for the compress kernel even when it has
+  // no work (the other idle CTAs leave at once and free their slots).
+  const bool keeps_order = blockIdx.x == 0 && blockIdx.y == 0;
+  if (grp.x < 0) {
+    if (keeps_order) griddep_wait();
+    return;
+  }
   const int row0 = grp.x, nrows = grp.y, req = grp.z;
   const int p_last = P.logical[row0 + nrows - 1];
   const int vmax = p_last < 0 ? 0 : (p_last + 1) / P.ratio;
   const int total_tiles = (vmax + 127) / 128;
   const int t_begin = blockIdx.y * P.tiles_per_cta;
   const int t_end = min(total_tiles, t_begin + P.tiles_per_cta);
-  if (t_begin >= t_end) return;
+  if (t_begin >= t_end) {
+    if (keeps_order) griddep_wait();
+    return;
+  }
   const int ntiles = t_end - t_begin;
 
   extern __shared__ uint8_t smem_raw[];
