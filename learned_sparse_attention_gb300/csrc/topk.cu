@@ -242,13 +242,17 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
 
 // ---------------------------------------------------------------------------
 // Register variant for V <= kRegKeys * kRegThreads (16384): thread t owns the
-// 32 consecutive blocks [32t, 32t + 32) and keeps their keys in registers.
+// kpt consecutive blocks [kpt t, kpt t + kpt) (kpt = V / 512 rounded up to a
+// multiple of 4, at most 32) and keeps their keys in registers, so every
+// thread shares the radix passes whatever V is.
 // Radix passes use per-warp private histograms (no cross-warp contention); the
 // final selection is a per-thread bit mask, so the ordered compaction is one
 // block scan of popcounts, ties going to the lower block by construction.
 constexpr int kRegThreads = 512;
 constexpr int kRegKeys = 32;
 constexpr int kRegWarps = kRegThreads / 32;
+constexpr int kCand = 2048;     // candidate buffer of the warp-level tail (shared memory)
+constexpr int kCandWarp = 256;  // the tail takes over once the chosen bin holds this few keys
 
 __device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
   __shared__ int sel[kRegKeys * kRegThreads / 4];  // K_b <= V / ... bounded by token_topk / r
   __shared__ int scratch[32];
   __shared__ uint32_t s_min[kRegWarps], s_max[kRegWarps];
-  __shared__ int s_digit, s_k;
+  __shared__ int s_digit, s_k, s_cnt;
 
   griddep_launch_dependents();
   if (P.tickets != nullptr && threadIdx.x < P.tickets_per_row)
@@ -304,24 +308,28 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
   }
   const bool take_all = V <= kb;
   if (!take_all) {
-    // keys of blocks [32 tid, 32 tid + 32); 0 marks "beyond V" (no real score maps to 0)
-    const int base = tid * kRegKeys;
+    // keys of blocks [kpt tid, kpt tid + kpt); 0 marks "beyond V" (no real
+    // score maps to 0)
+    const int kpt = min(kRegKeys, ((V + kRegThreads - 1) / kRegThreads + 3) & ~3);
+    const int base = tid * kpt;
     const float* lrow = P.logits + static_cast<long long>(row) * P.ld;
     uint32_t key[kRegKeys];
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
     for (int j = 0; j < kRegKeys; j += 4) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (base + j + 3 < V) v = *reinterpret_cast<const float4*>(lrow + base + j);
-      else {
-        if (base + j < V) v.x = lrow[base + j];
-        if (base + j + 1 < V) v.y = lrow[base + j + 1];
-        if (base + j + 2 < V) v.z = lrow[base + j + 2];
+      if (j < kpt) {
+        if (base + j + 3 < V) v = *reinterpret_cast<const float4*>(lrow + base + j);
+        else {
+          if (base + j < V) v.x = lrow[base + j];
+          if (base + j + 1 < V) v.y = lrow[base + j + 1];
+          if (base + j + 2 < V) v.z = lrow[base + j + 2];
+        }
       }
       const float f[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const bool ok = base + j + u < V;
+        const bool ok = j < kpt && base + j + u < V;
         key[j + u] = ok ? order_key(f[u]) : 0u;
         if (ok) {
           kmin = min(kmin, key[j + u]);
@@ -398,6 +406,7 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
           if (cum < k && k <= cum + cnt[j]) {
             s_digit = 255 - 8 * lane - j;
             s_k = k - cum;
+            s_cnt = cnt[j];
           }
           cum += cnt[j];
         }
@@ -407,6 +416,75 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
       pmask |= dmask << shift;
       k = s_k;
       hi = shift - 1;
+      if (hi >= 0 && s_cnt <= kCandWarp) {
+        // Few keys left in the chosen bin: gather them and let warp 0 finish
+        // the radix select with warp-level syncs only.
+        int mine = 0;
+#pragma unroll
+        for (int j = 0; j < kRegKeys; ++j) mine += (key[j] != 0u && (key[j] & pmask) == prefix) ? 1 : 0;
+        int ncand;
+        int at = block_sum_excl(mine, scratch, &ncand);
+        uint32_t* cand = reinterpret_cast<uint32_t*>(&whist[0][0]);    // kCand keys
+        int* h = &whist[kCand / 256][0];                                // 256 bins
+#pragma unroll
+        for (int j = 0; j < kRegKeys; ++j)
+          if (key[j] != 0u && (key[j] & pmask) == prefix) cand[at++] = key[j];
+        __syncthreads();
+        if (warp == 0) {
+          while (hi >= 0) {
+            const int width = hi + 1 < 8 ? hi + 1 : 8;
+            const int shift = hi - width + 1;
+            const uint32_t dmask = (1u << width) - 1u;
+#pragma unroll
+            for (int i = lane; i < 256; i += 32) h[i] = 0;
+            __syncwarp();
+            for (int i = lane; i < ncand; i += 32) {
+              const uint32_t c = cand[i];
+              if ((c & pmask) == prefix) atomicAdd(&h[(c >> shift) & dmask], 1);
+            }
+            __syncwarp();
+            int cnt[8], tot = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              cnt[j] = h[255 - 8 * lane - j];
+              tot += cnt[j];
+            }
+            int incl = tot;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+              const int y = __shfl_up_sync(0xffffffffu, incl, off);
+              if (lane >= off) incl += y;
+            }
+            int cum = incl - tot, digit = 0, knew = 0, found = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (cum < k && k <= cum + cnt[j]) {
+                digit = 255 - 8 * lane - j;
+                knew = k - cum;
+                found = 1;
+              }
+              cum += cnt[j];
+            }
+            const unsigned who = __ballot_sync(0xffffffffu, found);
+            const int src = who ? __ffs(who) - 1 : 0;
+            digit = __shfl_sync(0xffffffffu, digit, src);
+            knew = __shfl_sync(0xffffffffu, knew, src);
+            prefix |= static_cast<uint32_t>(digit) << shift;
+            pmask |= dmask << shift;
+            k = knew;
+            hi = shift - 1;
+            __syncwarp();
+          }
+          if (lane == 0) {
+            s_digit = static_cast<int>(prefix);
+            s_k = k;
+          }
+        }
+        __syncthreads();
+        prefix = static_cast<uint32_t>(s_digit);
+        k = s_k;
+        hi = -1;
+      }
     }
     const uint32_t T = prefix;
     const int keq = k;
@@ -416,15 +494,17 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
       gt_mask |= (key[j] > T ? 1u : 0u) << j;
       eq_mask |= (key[j] == T ? 1u : 0u) << j;
     }
+    // one scan of (greater, equal) counts: every greater key is taken and the
+    // first keq equal keys in block order
     int tot;
-    const int eq_before = block_sum_excl(__popc(eq_mask), scratch, &tot);
-    // keep the first keq equal keys in block order
+    const int both = block_sum_excl((__popc(gt_mask) << 16) | __popc(eq_mask), scratch, &tot);
+    const int gt_before = both >> 16, eq_before = both & 0xFFFF;
     int take = keq - eq_before;
     take = take < 0 ? 0 : take;
     uint32_t eq_take = eq_mask;
     for (int c = __popc(eq_mask); c > take; --c) eq_take &= ~(1u << (31 - __clz(eq_take)));
     uint32_t m = gt_mask | eq_take;
-    int out = block_sum_excl(__popc(m), scratch, &tot);
+    int out = gt_before + (eq_before < keq ? eq_before : keq);
     while (m) {
       const int j = __ffs(m) - 1;
       sel[out++] = base + j;
