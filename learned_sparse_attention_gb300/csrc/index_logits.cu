@@ -13,13 +13,14 @@
 //   warp 0      allocates TMEM, loads the B tile with one TMA box and issues
 //               tcgen05.mma (one thread) into two accumulator buffers so the
 //               epilogue overlaps the next tile;
-//   warps 1-4   A-tile producers: thread m copies key row m of each 128-key
-//               tile with 16-byte cp.async straight into the 128-byte
-//               swizzled K-major layout, through a 4-stage ring.  The keys of
-//               a tile sit on 128 / cpage scattered compressed pages (2 KB
-//               each for e4m3 and 16-key pages); one TMA box per page was
-//               measured to cap a CTA at ~1 tile per 0.9 us, so the gather
-//               uses cp.async and TMA keeps the one large box (B);
+//   warps 1-4   A-tile producers: 16-byte cp.async straight into the
+//               128-byte-swizzled K-major layout, through a ring of 3 (N <= 64)
+//               to 8 stages.  The keys of a tile sit on 128 / cpage scattered
+//               compressed pages (2 KB each for e4m3 and 16-key pages); one
+//               TMA box per page was measured at ~240 cycles of issue per box,
+//               so the gather uses cp.async and TMA keeps the one large box
+//               (B).  Lanes cover whole key rows for e4m3 at N <= 64, one key
+//               row per thread otherwise (see COALESCED);
 //   warps 5..   epilogue: one wide tcgen05.ld of the accumulator, branch-free
 //               ReLU / head sums, scale, coalesced fp32 stores.
 // Every wait is bounded (see mbar_wait); a timeout sets the error word.
@@ -50,7 +51,12 @@ struct LogitsCfg {
   // ReLU + head sums are chains of dependent adds, and only several warps
   // per scheduler hide their latency behind the MMA of the next tile
   static constexpr int EPI_WG = NPAD >= 128 ? NPAD / 64 : 1;
-  static constexpr int PRODUCERS = 128;                 // one thread per key row
+  static constexpr int PRODUCERS = 128;                 // producer threads (128 key rows a tile)
+  // Copy mapping of the A gather.  Lanes on whole key rows (every fetched
+  // 32-byte sector used in full) measured faster for e4m3 keys streamed from
+  // HBM at N <= 64 (decode); one key row per thread measured faster for bf16
+  // keys and for the L2-resident keys of long prefill row groups.
+  static constexpr bool COALESCED = IDT == 1 && NPAD <= 64;
   static constexpr int THREADS = 32 + PRODUCERS + 128 * EPI_WG;
   static constexpr int KSTEPS = IDT == 1 ? 4 : 8;       // 32 bytes of K per MMA
   static constexpr uint32_t TMEM_COLS = 2 * NPAD;
@@ -200,16 +206,35 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
       const int s = i % C::STAGES;
       const uint32_t ph = (i / C::STAGES) & 1;
       if (!mbar_wait(&empty[s], ph ^ 1, err)) break;
-      const int key = (t_begin + i) * 128 + m;
-      const int phys = s_page[min(i * ppt + m / cpage, npages - 1)];
-      const bool ok = key < vmax && phys >= 0;
-      const uint8_t* src = P.ccache + (static_cast<long long>(ok ? phys : 0) * cpage + (m % cpage)) *
-                                          P.row_bytes;
-      uint8_t* dst = sA + s * C::A_STAGE + m * 128;
+      if constexpr (!C::COALESCED) {
+        const int key = (t_begin + i) * 128 + m;
+        const int phys = s_page[min(i * ppt + m / cpage, npages - 1)];
+        const bool ok = key < vmax && phys >= 0;
+        const uint8_t* src = P.ccache + (static_cast<long long>(ok ? phys : 0) * cpage + (m % cpage)) *
+                                            P.row_bytes;
+        uint8_t* dst = sA + s * C::A_STAGE + m * 128;
 #pragma unroll
-      for (int c = 0; c < CH; ++c)
-        cp_async16(dst + (c >> 3) * C::A_ATOM + (((c & 7) ^ (m & 7)) << 4), src + c * 16,
-                   ok ? 16u : 0u);
+        for (int c = 0; c < CH; ++c)
+          cp_async16(dst + (c >> 3) * C::A_ATOM + (((c & 7) ^ (m & 7)) << 4), src + c * 16,
+                     ok ? 16u : 0u);
+      } else {
+        // step c copies 16-byte chunk m % CH of key row c * (128 / CH) + m / CH:
+        // CH consecutive lanes cover one whole key row, so every 32-byte sector
+        // a warp fetches is used in full
+        const int chunk = m % CH;
+        uint8_t* dst0 = sA + s * C::A_STAGE + (chunk >> 3) * C::A_ATOM;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int row = c * (128 / CH) + m / CH;
+          const int key = (t_begin + i) * 128 + row;
+          const int phys = s_page[min(i * ppt + row / cpage, npages - 1)];
+          const bool ok = key < vmax && phys >= 0;
+          const uint8_t* src = P.ccache +
+                               (static_cast<long long>(ok ? phys : 0) * cpage + (row % cpage)) * P.row_bytes +
+                               chunk * 16;
+          cp_async16(dst0 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4), src, ok ? 16u : 0u);
+        }
+      }
       cp_async_commit();
       ++issued;
       if (i >= LAG) {
