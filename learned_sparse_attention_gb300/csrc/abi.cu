@@ -228,7 +228,12 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
 
   int R, npad;
   logits_grouping(cfg, rows, reqs, &R, &npad);
-  const int max_groups = max_groups_for(rows, reqs, R);
+  // Two row groups per CTA share each key tile when the groups are full
+  // (prefill-sized requests) and the e4m3 ring still fits beside two query
+  // tiles.
+  const int avg_rows = reqs > 0 ? (rows + reqs - 1) / reqs : 1;
+  const int G = (cfg->index_dtype == QSA_DTYPE_E4M3 && npad == 256 && avg_rows >= 2 * R) ? 2 : 1;
+  const int max_groups = max_groups_for(rows, reqs, R * G);
   LogitsParams p{};
   p.cblock_table = cblock_table;
   p.logical = logical_positions;
@@ -242,10 +247,15 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
   p.rows = rows;
   p.reqs = reqs;
   p.rows_per_group = R;
+  p.groups_per_cta = G;
   p.n_heads = cfg->n_heads;
   p.ratio = cfg->compress_ratio;
   p.scale = 1.0f / (static_cast<float>(cfg->n_heads) * sqrtf(128.0f));
   p.row_bytes = 128 * elem_bytes(cfg);
+  // One TMA box per compressed page needs pages of at least 8 keys (a box
+  // then starts on a 1024-byte boundary of the swizzled tile) and row
+  // coordinates within int32.
+  p.tma_a = (cfg->cpage >= 8 && static_cast<long long>(cpages) * cfg->cpage < (1ll << 31)) ? 1 : 0;
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
 
@@ -268,11 +278,17 @@ qsa_status launch_logits(const qsa_cfg* cfg, const LogitsParams& p, const void* 
                          int32_t rows, int npad, int chunks, int max_groups, bool pdl,
                          cudaStream_t stream) {
   const int eb = elem_bytes(cfg);
-  CUtensorMap tq;
+  CUtensorMap tq, tcc;
   if (!encode_rows_map(&tq, q_idx, eb, static_cast<long long>(rows) * cfg->n_heads, npad))
     return QSA_ERR_CUDA;
-  return cuda_status(
-      launch_index_logits(p, tq, cfg->index_dtype, npad, max_groups, chunks, stream, pdl));
+  if (p.tma_a) {
+    if (!encode_rows_map(&tcc, p.ccache, eb, static_cast<long long>(p.cpages) * p.cpage, p.cpage))
+      return QSA_ERR_CUDA;
+  } else {
+    tcc = tq;  // unused
+  }
+  return cuda_status(launch_index_logits(p, tq, tcc, cfg->index_dtype, npad, max_groups, chunks,
+                                         stream, pdl));
 }
 
 qsa_status do_logits(const qsa_cfg* cfg, const void* q_idx, const void* ccache, int32_t cpages,

@@ -13,14 +13,16 @@
 //   warp 0      allocates TMEM, loads the B tile with one TMA box and issues
 //               tcgen05.mma (one thread) into two accumulator buffers so the
 //               epilogue overlaps the next tile;
-//   warps 1-4   A-tile producers: 16-byte cp.async straight into the
-//               128-byte-swizzled K-major layout, through a ring of 3 (N <= 64)
-//               to 8 stages.  The keys of a tile sit on 128 / cpage scattered
-//               compressed pages (2 KB each for e4m3 and 16-key pages); one
-//               TMA box per page was measured at ~240 cycles of issue per box,
-//               so the gather uses cp.async and TMA keeps the one large box
-//               (B).  Lanes cover whole key rows for e4m3 at N <= 64, one key
-//               row per thread otherwise (see COALESCED);
+//   warps 1-4   A-tile producers, through a ring of 3 (N <= 64) to 8 stages.
+//               The keys of a tile sit on 128 / cpage scattered compressed
+//               pages (2 KB each for e4m3 and 16-key pages).  For pages of 8
+//               or more keys, warp 1 loads them with one TMA box per page
+//               (SW128, completing on the stage's mbarrier), one lane per
+//               box so the boxes of a tile are in flight together: the
+//               gather then leaves the SM's load/store pipe to the
+//               epilogue's stores.  Shorter pages use 16-byte cp.async
+//               straight into the swizzled layout (lanes on whole key rows
+//               for e4m3 at N <= 64, one key row per thread otherwise);
 //   warps 5..   epilogue: one wide tcgen05.ld of the accumulator, branch-free
 //               ReLU / head sums, scale, coalesced fp32 stores.
 // Every wait is bounded (see mbar_wait); a timeout sets the error word.
@@ -32,26 +34,34 @@
 namespace qsa {
 namespace {
 
-template <int IDT, int NPAD>
+// G: row groups per CTA.  With G = 2 a CTA runs two row groups of the same
+// request over one stream of key tiles: each A tile feeds two MMAs (one per
+// group, into the two TMEM accumulators in turn), which halves the A-tile
+// traffic per FLOP; the epilogue of one group overlaps the other group's MMA.
+// TMA: the A tiles come by TMA (one producer warp) rather than cp.async (four).
+template <int IDT, int NPAD, int G = 1, bool TMA = false>
 struct LogitsCfg {
   static constexpr int ATOMS = IDT == 1 ? 1 : 2;        // 128-byte K atoms per key row
   static constexpr int A_ATOM = 128 * 128;              // bytes of one atom of a 128-key tile
   static constexpr int A_STAGE = A_ATOM * ATOMS;
   static constexpr int B_ATOM = NPAD * 128;
-  static constexpr int B_BYTES = B_ATOM * ATOMS;
+  static constexpr int B_GROUP = B_ATOM * ATOMS;        // one row group's query tile
+  static constexpr int B_BYTES = B_GROUP * G;
+  static constexpr int MAX_ROWS = 64;                   // rows per CTA (G * rows per group)
   static constexpr int MAX_PAGES = 4096;                // page ids staged per CTA (at most)
   // decode-sized tiles (N <= 64) keep 3 stages so that 4 CTAs fit on an SM;
   // from N = 128 on a CTA has the SM to itself (TMEM, registers), and the A
   // ring takes what shared memory is left after B and the page ids (at most
   // 8 stages): the A tiles come from L2 and need many bytes in flight.
   static constexpr int SMEM_LIMIT = 226 * 1024;  // 227 KB per CTA, less static smem
-  static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - B_BYTES - 256 - 128 - MAX_PAGES * 4) / A_STAGE;
+  static constexpr int STAGES_FIT =
+      (SMEM_LIMIT - 1024 - B_BYTES - 256 - MAX_ROWS * 4 - MAX_PAGES * 4) / A_STAGE;
   static constexpr int STAGES = NPAD <= 64 ? 3 : (STAGES_FIT < 8 ? STAGES_FIT : 8);
   // from N = 128 on one epilogue warpgroup per 64 accumulator columns: the
   // ReLU + head sums are chains of dependent adds, and only several warps
   // per scheduler hide their latency behind the MMA of the next tile
   static constexpr int EPI_WG = NPAD >= 128 ? NPAD / 64 : 1;
-  static constexpr int PRODUCERS = 128;                 // producer threads (128 key rows a tile)
+  static constexpr int PRODUCERS = TMA ? 32 : 128;      // producer threads (cp.async: a key row each)
   // Copy mapping of the A gather.  Lanes on whole key rows (every fetched
   // 32-byte sector used in full) measured faster for e4m3 keys streamed from
   // HBM at N <= 64 (decode); one key row per thread measured faster for bf16
@@ -61,18 +71,20 @@ struct LogitsCfg {
   static constexpr int KSTEPS = IDT == 1 ? 4 : 8;       // 32 bytes of K per MMA
   static constexpr uint32_t TMEM_COLS = 2 * NPAD;
   // shared memory without the page-id array, which is sized per launch
-  static constexpr int SMEM_BASE = 1024 + STAGES * A_STAGE + B_BYTES + 256 + 32 * 4;
+  static constexpr int SMEM_BASE = 1024 + STAGES * A_STAGE + B_BYTES + 256 + MAX_ROWS * 4;
   static_assert(STAGES >= 3 && SMEM_BASE + MAX_PAGES * 4 <= SMEM_LIMIT, "shared memory");
 };
 
-template <int IDT, int NPAD>
-__global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
-    index_logits_kernel(const __grid_constant__ CUtensorMap tmap_q, const LogitsParams P) {
-  using C = LogitsCfg<IDT, NPAD>;
+template <int IDT, int NPAD, int G, bool TMA>
+__global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
+    index_logits_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                        const __grid_constant__ CUtensorMap tmap_cc, const LogitsParams P) {
+  using C = LogitsCfg<IDT, NPAD, G, TMA>;
   griddep_launch_dependents();
   // Everything up to griddep_wait reads only caller inputs (metadata, page
   // tables), so it overlaps the tail of the compress kernel.
-  const int4 grp = find_group(P.qsl, P.reqs, P.rows, P.rows_per_group, blockIdx.x, P.err);
+  const int R = P.rows_per_group;
+  const int4 grp = find_group(P.qsl, P.reqs, P.rows, R * G, blockIdx.x, P.err);
   // The kernels after this one rely on "logits complete" implying "compress
   // complete", so CTA (0, 0) waits for the compress kernel even when it has
   // no work (the other idle CTAs leave at once and free their slots).
@@ -92,6 +104,8 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
     return;
   }
   const int ntiles = t_end - t_begin;
+  const int ngroups = (nrows + R - 1) / R;  // row groups in this CTA (<= G)
+  const int nitems = ntiles * ngroups;      // work item j: key tile j / ngroups, group j % ngroups
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
@@ -104,13 +118,14 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   uint64_t* bar_q = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_q + 1);
   int* s_vis = reinterpret_cast<int*>(smem_raw + pad + C::STAGES * C::A_STAGE + C::B_BYTES + 256);
-  int* s_page = s_vis + 32;  // tiles_per_cta * (128 / cpage) entries
+  int* s_page = s_vis + C::MAX_ROWS;  // tiles_per_cta * (128 / cpage) entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cpage = P.cpage;
   const int32_t* bt_row = P.cblock_table + static_cast<long long>(req) * P.cbt_stride;
   // Prologue: the group's visible-block counts and the physical compressed
-  // pages of this CTA's key range (-1: beyond the table), resolved in parallel.
+  // pages of this CTA's key range (-1: beyond the group's keys, -2: an
+  // out-of-range page id, counted and read as zeros), resolved in parallel.
   const int ppt = 128 / cpage;  // pages per 128-key tile
   const int page0 = t_begin * ppt;
   const int npages = ntiles * ppt;  // <= tiles_per_cta * ppt <= MAX_PAGES (host)
@@ -122,7 +137,7 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
       phys = bt_row[lp];
       if (phys < 0 || phys >= P.cpages) {
         flag_error(P.err);
-        phys = -1;
+        phys = -2;
       }
     }
     s_page[i] = phys;
@@ -133,12 +148,12 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], C::PRODUCERS);
+      mbar_init(&full[s], TMA ? 1 : C::PRODUCERS);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 128 * C::EPI_WG);
+      mbar_init(&acc_empty[a], 4 * C::EPI_WG);  // one arrival per epilogue warp
     }
     mbar_init(bar_q, 1);
     fence_barrier_init();
@@ -158,41 +173,83 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
     // ------------------------------------------------------ B tile + MMA issuer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
-      mbar_arrive_expect_tx(bar_q, C::B_BYTES);
+      if (TMA) tma_prefetch_desc(&tmap_cc);
+      mbar_arrive_expect_tx(bar_q, ngroups * C::B_GROUP);
+      for (int g = 0; g < ngroups; ++g) {
 #pragma unroll
-      for (int atom = 0; atom < C::ATOMS; ++atom)
-        tma_load_2d(sB + atom * C::B_ATOM, &tmap_q, atom * 64, row0 * P.n_heads, bar_q);
-      uint32_t n_eff = ((nrows * P.n_heads + 31) / 32) * 32;
-      if (n_eff > NPAD) n_eff = NPAD;
-      const uint32_t idesc = umma_idesc(IDT == 1 ? 0u : 1u, 128, n_eff);
+        for (int atom = 0; atom < C::ATOMS; ++atom)
+          tma_load_2d(sB + g * C::B_GROUP + atom * C::B_ATOM, &tmap_q, atom * 64,
+                      (row0 + g * R) * P.n_heads, bar_q);
+      }
+      uint32_t idesc[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int rows_g = min(R, nrows - g * R);
+        uint32_t n_eff = ((max(rows_g, 1) * P.n_heads + 31) / 32) * 32;
+        if (n_eff > NPAD) n_eff = NPAD;
+        idesc[g] = umma_idesc(IDT == 1 ? 0u : 1u, 128, n_eff);
+      }
       bool ok = mbar_wait(bar_q, 0, err);
-      const uint32_t b_base = smem_addr(sB);
-      for (int i = 0; ok && i < ntiles; ++i) {
+      for (int j = 0; ok && j < nitems; ++j) {
+        const int i = j / ngroups, g = j - i * ngroups;
         const int s = i % C::STAGES;
         const uint32_t ph = (i / C::STAGES) & 1;
-        const int a = i & 1;
-        const uint32_t aph = (i >> 1) & 1;
+        const int a = j & 1;
+        const uint32_t aph = (j >> 1) & 1;
         if (!mbar_wait(&acc_empty[a], aph ^ 1, err)) break;
-        if (!mbar_wait(&full[s], ph, err)) break;
+        if (g == 0 && !mbar_wait(&full[s], ph, err)) break;
         tc_fence_after_sync();
         const uint32_t a_base = smem_addr(sA + s * C::A_STAGE);
+        const uint32_t b_base = smem_addr(sB + g * C::B_GROUP);
         const uint32_t d_tmem = tmem_base + a * NPAD;
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
           const uint32_t atom = kk >> 2, koff = (kk & 3) * 32;
           const uint64_t adesc = umma_sdesc_sw128(a_base + atom * C::A_ATOM + koff);
           const uint64_t bdesc = umma_sdesc_sw128(b_base + atom * C::B_ATOM + koff);
+          const uint32_t id = G == 1 ? idesc[0] : idesc[g];
           if (IDT == 1)
-            umma_f8f6f4(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+            umma_f8f6f4(d_tmem, adesc, bdesc, id, kk > 0 ? 1u : 0u);
           else
-            umma_f16(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+            umma_f16(d_tmem, adesc, bdesc, id, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&empty[s]);
+        if (g == ngroups - 1) umma_commit(&empty[s]);  // the tile's last reader
         umma_commit(&acc_full[a]);
       }
     }
     __syncwarp();
-  } else if (warp <= C::PRODUCERS / 32) {
+  } else if (TMA && warp == 1) {
+    // ------------------------------------------------------ A tiles by TMA
+    // Warp 1: box b of a tile = page b % ppt, 128-byte K atom b / ppt.  Lane
+    // 0 arms the stage's barrier with the bytes of the valid boxes, then
+    // every lane issues its box.  Pages past the group's keys are skipped
+    // (those rows are never stored); an out-of-range page id is read as
+    // zeros, written before the barrier is armed.
+    if (warp == 1) {
+      const int nbox = C::ATOMS * ppt;  // <= 32 for cpage >= 8
+      const uint32_t box_bytes = static_cast<uint32_t>(cpage) * 128u;
+      const int elems_per_atom = 128 / (IDT == 1 ? 1 : 2);
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % C::STAGES;
+        const uint32_t ph = (i / C::STAGES) & 1;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int j = lane % ppt, atom = lane / ppt;
+        const int phys = lane < nbox ? s_page[i * ppt + j] : -1;
+        uint8_t* dst = sA + s * C::A_STAGE + atom * C::A_ATOM + j * cpage * 128;
+        if (phys == -2) {
+          for (uint32_t o = 0; o < box_bytes; o += 16)
+            *reinterpret_cast<uint4*>(dst + o) = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+        }
+        const unsigned valid = __ballot_sync(0xffffffffu, phys >= 0);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(valid) * box_bytes);
+        __syncwarp();
+        if (phys >= 0) tma_load_2d(dst, &tmap_cc, atom * elems_per_atom, phys * cpage, &full[s]);
+      }
+    }
+  } else if (!TMA && warp <= C::PRODUCERS / 32) {
     // ------------------------------------------------------ A-tile producers
     // Thread m copies key row m of every tile: 8 (e4m3) or 16 (bf16) 16-byte
     // cp.async into the 128-byte-swizzled K-major layout the MMA reads.  A
@@ -251,50 +308,60 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
     const int wg = (warp - 1 - C::PRODUCERS / 32) >> 2;
     const int lane_base = 32 * (warp & 3);
     const int m = lane_base + lane;
-    const int cols = nrows * P.n_heads;
     const int col_begin = wg * (NPAD / C::EPI_WG);
-    const int col_end = min(cols, col_begin + NPAD / C::EPI_WG);
     constexpr int COLS = NPAD / C::EPI_WG;  // accumulator columns of this warpgroup
-    for (int i = 0; i < ntiles; ++i) {
-      const int a = i & 1;
-      const uint32_t aph = (i >> 1) & 1;
+    constexpr int NSEG = COLS / 8;
+    // This warpgroup's rows of each group, their visible counts and output
+    // rows are fixed for the CTA: kept in registers, so that the item loop
+    // touches shared memory only through one barrier arrival per warp.
+    const int r0 = col_begin / P.n_heads;
+    int vis[G][NSEG];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int rows_g = min(R, nrows - g * R);
+      const int rows_here = max(0, min(rows_g * P.n_heads, col_begin + COLS) - col_begin) / P.n_heads;
+#pragma unroll
+      for (int q = 0; q < NSEG; ++q) vis[g][q] = q < rows_here ? s_vis[g * R + r0 + q] : 0;
+    }
+    float* const out0 = P.logits + static_cast<long long>(row0 + r0) * P.ld;
+    for (int j = 0; j < nitems; ++j) {
+      const int i = j / ngroups, g = j - i * ngroups;
+      const int a = j & 1;
+      const uint32_t aph = (j >> 1) & 1;
       if (!mbar_wait(&acc_full[a], aph, err)) break;
       tc_fence_after_sync();
       const int key = (t_begin + i) * 128 + m;
-      // The warpgroup's columns in 32-column TMEM reads, double-buffered so
-      // that the next read is in flight while the current one is summed.  An
-      // 8-column segment is relu-summed with max(x, 0) on five columns (ALU
-      // pipe) and (x + |x|) / 2 on three (FMA pipe), which keeps the two
-      // pipes about equally loaded; then the accumulator goes straight back
-      // to the MMA warp, and the head sums and stores follow.
+      // The warpgroup's columns in 32-column TMEM reads (the other epilogue
+      // warps hide each read's latency).  An 8-column segment is relu-summed
+      // with max(x, 0) on five columns (ALU pipe) and (x + |x|) / 2 on three
+      // (FMA pipe), which keeps the two pipes about equally loaded; then the
+      // accumulator goes straight back to the MMA warp, and the head sums
+      // and stores follow.
       constexpr int NCH = COLS / 32;
-      constexpr int NSEG = COLS / 8;
       float seg[NSEG];
-      uint32_t buf[2][32];
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_base) << 16) + a * NPAD + col_begin;
-      tmem_ld32_issue(taddr, buf[0]);
-      tmem_wait_ld32(buf[0]);
 #pragma unroll
       for (int h = 0; h < NCH; ++h) {
-        if (h + 1 < NCH) tmem_ld32_issue(taddr + (h + 1) * 32, buf[(h + 1) & 1]);
+        uint32_t x[32];
+        tmem_ld32_issue(taddr + h * 32, x);
+        tmem_wait_ld32(x);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t* x = &buf[h & 1][q * 8];
           float t = 0.f, u = 0.f, w = 0.f;
 #pragma unroll
-          for (int e = 0; e < 5; ++e) t += fmaxf(__uint_as_float(x[e]), 0.f);
+          for (int e = 0; e < 5; ++e) t += fmaxf(__uint_as_float(x[q * 8 + e]), 0.f);
 #pragma unroll
           for (int e = 5; e < 8; ++e) {
-            const float f = __uint_as_float(x[e]);
+            const float f = __uint_as_float(x[q * 8 + e]);
             u += f;
             w += fabsf(f);
           }
           seg[h * 4 + q] = fmaf(0.5f, u + w, t);
         }
-        if (h + 1 < NCH) tmem_wait_ld32(buf[(h + 1) & 1]);
       }
       tc_fence_before_sync();
-      mbar_arrive_relaxed(&acc_empty[a]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_relaxed(&acc_empty[a]);
       // pairwise tree up to n_heads columns per row (n_heads is 8, 16, 32
       // or 64): branch-free, compact.
       if (P.n_heads >= 16) {
@@ -309,15 +376,10 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
 #pragma unroll
         for (int q = 0; q < NSEG / 8; ++q) seg[q] = seg[2 * q] + seg[2 * q + 1];
       }
-      const int rows_here = max(0, col_end - col_begin) / P.n_heads;
-      const int r0 = col_begin / P.n_heads;
 #pragma unroll
       for (int q = 0; q < NSEG; ++q) {
-        if (q < rows_here) {
-          const int r = r0 + q;
-          if (r < nrows && key < s_vis[r])
-            P.logits[static_cast<long long>(row0 + r) * P.ld + key] = seg[q] * P.scale;
-        }
+        const int v = (G == 1 || g == 0) ? vis[0][q] : vis[G - 1][q];
+        if (key < v) out0[(g * R + q) * P.ld + key] = seg[q] * P.scale;
       }
     }
   }
@@ -329,11 +391,11 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD>::THREADS, 1)
   }
 }
 
-template <int IDT, int NPAD>
-cudaError_t launch_one(const LogitsParams& p, const CUtensorMap& tq, int max_groups, int chunks,
-                       cudaStream_t stream, bool pdl) {
-  using C = LogitsCfg<IDT, NPAD>;
-  auto kern = index_logits_kernel<IDT, NPAD>;
+template <int IDT, int NPAD, int G, bool TMA>
+cudaError_t launch_cfg(const LogitsParams& p, const CUtensorMap& tq, const CUtensorMap& tcc,
+                       int max_groups, int chunks, cudaStream_t stream, bool pdl) {
+  using C = LogitsCfg<IDT, NPAD, G, TMA>;
+  auto kern = index_logits_kernel<IDT, NPAD, G, TMA>;
   const int smem = C::SMEM_BASE + p.tiles_per_cta * (128 / p.cpage) * 4;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -348,28 +410,40 @@ cudaError_t launch_one(const LogitsParams& p, const CUtensorMap& tq, int max_gro
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  return launch_kernel(kern, dim3(max_groups, chunks), dim3(C::THREADS), smem, stream, pdl, tq, p);
+  return launch_kernel(kern, dim3(max_groups, chunks), dim3(C::THREADS), smem, stream, pdl, tq, tcc,
+                       p);
+}
+
+template <int IDT, int NPAD>
+cudaError_t launch_one(const LogitsParams& p, const CUtensorMap& tq, const CUtensorMap& tcc,
+                       int max_groups, int chunks, cudaStream_t stream, bool pdl) {
+  if (!p.tma_a) return launch_cfg<IDT, NPAD, 1, false>(p, tq, tcc, max_groups, chunks, stream, pdl);
+  if constexpr (IDT == 1 && NPAD == 256) {
+    if (p.groups_per_cta == 2)
+      return launch_cfg<IDT, NPAD, 2, true>(p, tq, tcc, max_groups, chunks, stream, pdl);
+  }
+  return launch_cfg<IDT, NPAD, 1, true>(p, tq, tcc, max_groups, chunks, stream, pdl);
 }
 
 }  // namespace
 
-cudaError_t launch_index_logits(const LogitsParams& p, const CUtensorMap& tq, int index_dtype,
-                                int npad, int max_groups, int chunks, cudaStream_t stream,
-                                bool pdl) {
+cudaError_t launch_index_logits(const LogitsParams& p, const CUtensorMap& tq,
+                                const CUtensorMap& tcc, int index_dtype, int npad,
+                                int max_groups, int chunks, cudaStream_t stream, bool pdl) {
   if (max_groups <= 0 || chunks <= 0) return cudaSuccess;
   if (index_dtype == 1) {
     switch (npad) {
-      case 32: return launch_one<1, 32>(p, tq, max_groups, chunks, stream, pdl);
-      case 64: return launch_one<1, 64>(p, tq, max_groups, chunks, stream, pdl);
-      case 128: return launch_one<1, 128>(p, tq, max_groups, chunks, stream, pdl);
-      case 256: return launch_one<1, 256>(p, tq, max_groups, chunks, stream, pdl);
+      case 32: return launch_one<1, 32>(p, tq, tcc, max_groups, chunks, stream, pdl);
+      case 64: return launch_one<1, 64>(p, tq, tcc, max_groups, chunks, stream, pdl);
+      case 128: return launch_one<1, 128>(p, tq, tcc, max_groups, chunks, stream, pdl);
+      case 256: return launch_one<1, 256>(p, tq, tcc, max_groups, chunks, stream, pdl);
     }
   } else {
     switch (npad) {
-      case 32: return launch_one<0, 32>(p, tq, max_groups, chunks, stream, pdl);
-      case 64: return launch_one<0, 64>(p, tq, max_groups, chunks, stream, pdl);
-      case 128: return launch_one<0, 128>(p, tq, max_groups, chunks, stream, pdl);
-      case 256: return launch_one<0, 256>(p, tq, max_groups, chunks, stream, pdl);
+      case 32: return launch_one<0, 32>(p, tq, tcc, max_groups, chunks, stream, pdl);
+      case 64: return launch_one<0, 64>(p, tq, tcc, max_groups, chunks, stream, pdl);
+      case 128: return launch_one<0, 128>(p, tq, tcc, max_groups, chunks, stream, pdl);
+      case 256: return launch_one<0, 256>(p, tq, tcc, max_groups, chunks, stream, pdl);
     }
   }
   return cudaErrorInvalidValue;

@@ -49,14 +49,19 @@ struct LogitsParams {
   float scale;
   int tiles_per_cta;
   int row_bytes;
+  int tma_a;  // gather the key tiles with one TMA box per compressed page (cpage >= 8)
+  int groups_per_cta;  // 1, or 2 (e4m3, N = 256): two row groups share each key tile
   unsigned long long* err;
 };
 
 // npad: padded MMA N (32, 64, 128 or 256); grid = (max_groups, chunks), CTA
-// x handles row group x (each request's rows in chunks of rows_per_group).
-cudaError_t launch_index_logits(const LogitsParams& p, const CUtensorMap& tmap_q, int index_dtype,
-                                int npad, int max_groups, int chunks, cudaStream_t stream,
-                                bool pdl);
+// x handles row group x (each request's rows in chunks of rows_per_group *
+// groups_per_cta).
+// tmap_cc: the compressed cache as [cpages * cpage rows, 128 elements] with a
+// box of cpage rows x 128 bytes (used when p.tma_a).
+cudaError_t launch_index_logits(const LogitsParams& p, const CUtensorMap& tmap_q,
+                                const CUtensorMap& tmap_cc, int index_dtype, int npad,
+                                int max_groups, int chunks, cudaStream_t stream, bool pdl);
 
 struct TopkParams {
   const float* logits;

@@ -37,6 +37,24 @@ MID = {
     "mid_h64_e4m3_r2": W.small_spec("mid_h64_e4m3_r2", seed=14, contexts=(5000, 300),
                                     rows_per_req=(2, 1), n_heads=64, index_dtype=E4,
                                     compress_ratio=2, token_topk=256, hq=64, hkv=8, page=16),
+    # row groups of 32 rows x 8 heads and 16 rows x 16 heads (256 MMA columns)
+    "mid_h8_rows32_bf16": W.small_spec("mid_h8_rows32_bf16", seed=15, contexts=(2000, 3001),
+                                       rows_per_req=(32, 21), n_heads=8, index_dtype=BF,
+                                       compress_ratio=4, token_topk=256, hq=8, hkv=1, page=32),
+    "mid_h16_rows16_e4m3": W.small_spec("mid_h16_rows16_e4m3", seed=16,
+                                        contexts=(4000, 1501, 903), rows_per_req=(16, 9, 16),
+                                        n_heads=16, index_dtype=E4, compress_ratio=4,
+                                        token_topk=512, hq=16, hkv=2, page=64),
+    # two row groups per logits CTA (e4m3, 256 MMA columns, >= 2 full groups
+    # per request on average), with partial second groups
+    "mid_e4m3_h32_two_groups": W.small_spec("mid_e4m3_h32_two_groups", seed=17,
+                                            contexts=(3000, 2101), rows_per_req=(40, 23),
+                                            n_heads=32, index_dtype=E4, compress_ratio=4,
+                                            token_topk=512, hq=32, hkv=4, page=64),
+    "mid_e4m3_h8_two_groups": W.small_spec("mid_e4m3_h8_two_groups", seed=18,
+                                           contexts=(1500, 2603), rows_per_req=(70, 66),
+                                           n_heads=8, index_dtype=E4, compress_ratio=4,
+                                           token_topk=256, hq=8, hkv=1, page=32),
 }
 
 
