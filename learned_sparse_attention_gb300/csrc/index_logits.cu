@@ -190,24 +190,27 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
         idesc[g] = umma_idesc(IDT == 1 ? 0u : 1u, 128, n_eff);
       }
       bool ok = mbar_wait(bar_q, 0, err);
+      // smem descriptors: the start-address field (address / 16, 14 bits)
+      // takes byte offsets / 16 without carrying out (shared memory < 256 KB)
+      const uint64_t a_desc0 = umma_sdesc_sw128(smem_addr(sA));
+      const uint64_t b_desc0 = umma_sdesc_sw128(smem_addr(sB));
+      int g = 0, s = 0;
+      uint32_t ph = 0;
       for (int j = 0; ok && j < nitems; ++j) {
-        const int i = j / ngroups, g = j - i * ngroups;
-        const int s = i % C::STAGES;
-        const uint32_t ph = (i / C::STAGES) & 1;
         const int a = j & 1;
         const uint32_t aph = (j >> 1) & 1;
         if (!mbar_wait(&acc_empty[a], aph ^ 1, err)) break;
         if (g == 0 && !mbar_wait(&full[s], ph, err)) break;
         tc_fence_after_sync();
-        const uint32_t a_base = smem_addr(sA + s * C::A_STAGE);
-        const uint32_t b_base = smem_addr(sB + g * C::B_GROUP);
+        const uint64_t a_desc = a_desc0 + ((s * C::A_STAGE) >> 4);
+        const uint64_t b_desc = b_desc0 + ((g * C::B_GROUP) >> 4);
         const uint32_t d_tmem = tmem_base + a * NPAD;
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
-          const uint32_t atom = kk >> 2, koff = (kk & 3) * 32;
-          const uint64_t adesc = umma_sdesc_sw128(a_base + atom * C::A_ATOM + koff);
-          const uint64_t bdesc = umma_sdesc_sw128(b_base + atom * C::B_ATOM + koff);
-          const uint32_t id = G == 1 ? idesc[0] : idesc[g];
+          const uint32_t off = (kk & 3) * 32;  // byte offset inside a 128-byte K atom
+          const uint64_t adesc = a_desc + (((kk >> 2) * C::A_ATOM + off) >> 4);
+          const uint64_t bdesc = b_desc + (((kk >> 2) * C::B_ATOM + off) >> 4);
+          const uint32_t id = (G == 1 || g == 0) ? idesc[0] : idesc[G - 1];
           if (IDT == 1)
             umma_f8f6f4(d_tmem, adesc, bdesc, id, kk > 0 ? 1u : 0u);
           else
@@ -215,6 +218,13 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
         }
         if (g == ngroups - 1) umma_commit(&empty[s]);  // the tile's last reader
         umma_commit(&acc_full[a]);
+        if (++g == ngroups) {  // next key tile
+          g = 0;
+          if (++s == C::STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
       }
     }
     __syncwarp();
@@ -323,9 +333,15 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
 #pragma unroll
       for (int q = 0; q < NSEG; ++q) vis[g][q] = q < rows_here ? s_vis[g * R + r0 + q] : 0;
     }
+    int live[G];  // rows of each group held by this warpgroup
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int rows_g = min(R, nrows - g * R);
+      live[g] = max(0, min(rows_g * P.n_heads, col_begin + COLS) - col_begin) / P.n_heads;
+    }
     float* const out0 = P.logits + static_cast<long long>(row0 + r0) * P.ld;
+    int i = 0, g = 0;
     for (int j = 0; j < nitems; ++j) {
-      const int i = j / ngroups, g = j - i * ngroups;
       const int a = j & 1;
       const uint32_t aph = (j >> 1) & 1;
       if (!mbar_wait(&acc_full[a], aph, err)) break;
@@ -333,12 +349,14 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
       const int key = (t_begin + i) * 128 + m;
       // The warpgroup's columns in 32-column TMEM reads (the other epilogue
       // warps hide each read's latency).  An 8-column segment is relu-summed
-      // with max(x, 0) on five columns (ALU pipe) and (x + |x|) / 2 on three
-      // (FMA pipe), which keeps the two pipes about equally loaded; then the
-      // accumulator goes straight back to the MMA warp, and the head sums
-      // and stores follow.
+      // as four pairs of max(x, 0) added with packed f32x2 adds: measured,
+      // this leaves the tensor pipe at full rate beside the epilogue, where
+      // scalar max/add/abs chains starved the MMA-issuing warp of issue slots
+      // (~2x slower MMAs).  The accumulator goes straight back to the MMA
+      // warp, then the head sums (packed pairs, one final add per row) and
+      // the stores follow.
       constexpr int NCH = COLS / 32;
-      float seg[NSEG];
+      unsigned long long seg[NSEG];
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_base) << 16) + a * NPAD + col_begin;
 #pragma unroll
       for (int h = 0; h < NCH; ++h) {
@@ -347,16 +365,12 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
         tmem_wait_ld32(x);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float t = 0.f, u = 0.f, w = 0.f;
+          unsigned long long pr[4];
 #pragma unroll
-          for (int e = 0; e < 5; ++e) t += fmaxf(__uint_as_float(x[q * 8 + e]), 0.f);
-#pragma unroll
-          for (int e = 5; e < 8; ++e) {
-            const float f = __uint_as_float(x[q * 8 + e]);
-            u += f;
-            w += fabsf(f);
-          }
-          seg[h * 4 + q] = fmaf(0.5f, u + w, t);
+          for (int e = 0; e < 4; ++e)
+            pr[e] = f32x2_pack(fmaxf(__uint_as_float(x[q * 8 + 2 * e]), 0.f),
+                               fmaxf(__uint_as_float(x[q * 8 + 2 * e + 1]), 0.f));
+          seg[h * 4 + q] = f32x2_add(f32x2_add(pr[0], pr[1]), f32x2_add(pr[2], pr[3]));
         }
       }
       tc_fence_before_sync();
@@ -366,20 +380,26 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
       // or 64): branch-free, compact.
       if (P.n_heads >= 16) {
 #pragma unroll
-        for (int q = 0; q < NSEG / 2; ++q) seg[q] = seg[2 * q] + seg[2 * q + 1];
+        for (int q = 0; q < NSEG / 2; ++q) seg[q] = f32x2_add(seg[2 * q], seg[2 * q + 1]);
       }
       if (P.n_heads >= 32) {
 #pragma unroll
-        for (int q = 0; q < NSEG / 4; ++q) seg[q] = seg[2 * q] + seg[2 * q + 1];
+        for (int q = 0; q < NSEG / 4; ++q) seg[q] = f32x2_add(seg[2 * q], seg[2 * q + 1]);
       }
       if (P.n_heads >= 64) {
 #pragma unroll
-        for (int q = 0; q < NSEG / 8; ++q) seg[q] = seg[2 * q] + seg[2 * q + 1];
+        for (int q = 0; q < NSEG / 8; ++q) seg[q] = f32x2_add(seg[2 * q], seg[2 * q + 1]);
       }
+      const int nlive = (G == 1 || g == 0) ? live[0] : live[G - 1];
 #pragma unroll
       for (int q = 0; q < NSEG; ++q) {
+        if (q >= nlive) break;  // uniform across the warpgroup
         const int v = (G == 1 || g == 0) ? vis[0][q] : vis[G - 1][q];
-        if (key < v) out0[(g * R + q) * P.ld + key] = seg[q] * P.scale;
+        if (key < v) out0[(g * R + q) * P.ld + key] = f32x2_hsum(seg[q]) * P.scale;
+      }
+      if (++g == ngroups) {
+        g = 0;
+        ++i;
       }
     }
   }

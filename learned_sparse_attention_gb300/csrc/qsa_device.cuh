@@ -247,6 +247,26 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// ---------------------------------------------------------------- f32 pairs
+// Two fp32 values in one 64-bit register pair, for the packed add.f32x2 of
+// sm_100+ (one instruction for two sums).
+__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f32x2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// lo + hi of a pair
+__device__ __forceinline__ float f32x2_hsum(unsigned long long a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return lo + hi;
+}
+
 // ---------------------------------------------------------------- formats
 // Two floats -> two e4m3 bytes (round to nearest even, saturate to +-448);
 // `lo` lands in the low byte.
