@@ -61,6 +61,7 @@ struct LogitsCfg {
   // ReLU + head sums are chains of dependent adds, and only several warps
   // per scheduler hide their latency behind the MMA of the next tile
   static constexpr int EPI_WG = NPAD >= 128 ? NPAD / 64 : 1;
+  static constexpr int TEAMS = EPI_WG >= 2 ? 2 : 1;     // epilogue teams taking items in turn
   static constexpr int PRODUCERS = TMA ? 32 : 128;      // producer threads (cp.async: a key row each)
   // Copy mapping of the A gather.  Lanes on whole key rows (every fetched
   // 32-byte sector used in full) measured faster for e4m3 keys streamed from
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4 * C::EPI_WG);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[a], 4 * (C::EPI_WG / C::TEAMS));  // one arrival per warp of a team
     }
     mbar_init(bar_q, 1);
     fence_barrier_init();
@@ -315,46 +316,42 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
     for (int i = max(0, issued - LAG); i < issued; ++i) mbar_arrive(&full[i % C::STAGES]);
   } else {
     // ------------------------------------------------------------ epilogue
+    // The epilogue warpgroups form C::TEAMS teams that take the items in
+    // turn: team t handles items t, t + TEAMS, ...  With two teams each team
+    // owns one TMEM accumulator (and, with two row groups per CTA, one
+    // group), so one team's wait for its next accumulator overlaps the other
+    // team's work.
+    constexpr int WGT = C::EPI_WG / C::TEAMS;  // warpgroups per team
+    constexpr int COLS = NPAD / WGT;           // accumulator columns of a warpgroup
+    constexpr int NSEG = COLS / 8;
     const int wg = (warp - 1 - C::PRODUCERS / 32) >> 2;
+    const int team = wg / WGT;
     const int lane_base = 32 * (warp & 3);
     const int m = lane_base + lane;
-    const int col_begin = wg * (NPAD / C::EPI_WG);
-    constexpr int COLS = NPAD / C::EPI_WG;  // accumulator columns of this warpgroup
-    constexpr int NSEG = COLS / 8;
-    // This warpgroup's rows of each group, their visible counts and output
-    // rows are fixed for the CTA: kept in registers, so that the item loop
-    // touches shared memory only through one barrier arrival per warp.
+    const int col_begin = (wg % WGT) * COLS;
     const int r0 = col_begin / P.n_heads;
-    int vis[G][NSEG];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const int rows_g = min(R, nrows - g * R);
-      const int rows_here = max(0, min(rows_g * P.n_heads, col_begin + COLS) - col_begin) / P.n_heads;
-#pragma unroll
-      for (int q = 0; q < NSEG; ++q) vis[g][q] = q < rows_here ? s_vis[g * R + r0 + q] : 0;
-    }
-    int live[G];  // rows of each group held by this warpgroup
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const int rows_g = min(R, nrows - g * R);
-      live[g] = max(0, min(rows_g * P.n_heads, col_begin + COLS) - col_begin) / P.n_heads;
-    }
-    float* const out0 = P.logits + static_cast<long long>(row0 + r0) * P.ld;
-    int i = 0, g = 0;
-    for (int j = 0; j < nitems; ++j) {
+    // the row group of this team's items (two teams, two groups: team t has
+    // group t; otherwise every item is group 0)
+    const int gq = (C::TEAMS == 2 && ngroups == 2) ? team : 0;
+    const int rows_g = min(R, nrows - gq * R);
+    const int nlive = max(0, min(rows_g * P.n_heads, col_begin + COLS) - col_begin) / P.n_heads;
+    const int* vis = s_vis + gq * R + r0;
+    float* const out0 = P.logits + static_cast<long long>(row0 + gq * R + r0) * P.ld;
+    for (int j = team; j < nitems; j += C::TEAMS) {
       const int a = j & 1;
       const uint32_t aph = (j >> 1) & 1;
+      const int i = ngroups == 2 ? (j >> 1) : j;  // key tile of item j
       if (!mbar_wait(&acc_full[a], aph, err)) break;
       tc_fence_after_sync();
       const int key = (t_begin + i) * 128 + m;
       // The warpgroup's columns in 32-column TMEM reads (the other epilogue
-      // warps hide each read's latency).  An 8-column segment is relu-summed
-      // as four pairs of max(x, 0) added with packed f32x2 adds: measured,
-      // this leaves the tensor pipe at full rate beside the epilogue, where
-      // scalar max/add/abs chains starved the MMA-issuing warp of issue slots
-      // (~2x slower MMAs).  The accumulator goes straight back to the MMA
-      // warp, then the head sums (packed pairs, one final add per row) and
-      // the stores follow.
+      // warps hide each read's latency).  relu(x) is summed as x + |x| (one
+      // FMA-pipe add with an absolute-value operand; the factor 1/2 is folded
+      // into the scale) over pairs added with packed f32x2 adds.  Measured:
+      // max(x, 0) on the ALU pipe saturated it beside the MMA-issuing warp's
+      // integer work, and scalar add chains starved that warp of issue slots.
+      // The accumulator goes straight back to the MMA warp, then the head sums
+      // (packed pairs, one final add per row) and the stores follow.
       constexpr int NCH = COLS / 32;
       unsigned long long seg[NSEG];
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lane_base) << 16) + a * NPAD + col_begin;
@@ -367,9 +364,11 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
         for (int q = 0; q < 4; ++q) {
           unsigned long long pr[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            pr[e] = f32x2_pack(fmaxf(__uint_as_float(x[q * 8 + 2 * e]), 0.f),
-                               fmaxf(__uint_as_float(x[q * 8 + 2 * e + 1]), 0.f));
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = __uint_as_float(x[q * 8 + 2 * e]);
+            const float x1 = __uint_as_float(x[q * 8 + 2 * e + 1]);
+            pr[e] = f32x2_pack(x0 + fabsf(x0), x1 + fabsf(x1));  // 2 relu(x)
+          }
           seg[h * 4 + q] = f32x2_add(f32x2_add(pr[0], pr[1]), f32x2_add(pr[2], pr[3]));
         }
       }
@@ -390,16 +389,10 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
 #pragma unroll
         for (int q = 0; q < NSEG / 8; ++q) seg[q] = f32x2_add(seg[2 * q], seg[2 * q + 1]);
       }
-      const int nlive = (G == 1 || g == 0) ? live[0] : live[G - 1];
 #pragma unroll
       for (int q = 0; q < NSEG; ++q) {
         if (q >= nlive) break;  // uniform across the warpgroup
-        const int v = (G == 1 || g == 0) ? vis[0][q] : vis[G - 1][q];
-        if (key < v) out0[(g * R + q) * P.ld + key] = f32x2_hsum(seg[q]) * P.scale;
-      }
-      if (++g == ngroups) {
-        g = 0;
-        ++i;
+        if (key < vis[q]) out0[q * P.ld + key] = f32x2_hsum(seg[q]) * (0.5f * P.scale);
       }
     }
   }
