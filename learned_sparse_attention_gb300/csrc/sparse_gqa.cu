@@ -119,6 +119,15 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     qb[kk][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t);
     qb[kk][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t);
   }
+  // The request's block-table row (a caller input) goes to the pipeline
+  // buffers before the wait, so that resolving the selected tokens' pages
+  // after it costs shared-memory reads instead of a second round trip to
+  // global memory.  Rows longer than the buffers read the table directly.
+  const int32_t* bt_row = P.block_table + static_cast<long long>(req < 0 ? 0 : req) * P.bt_stride;
+  int32_t* s_bt = reinterpret_cast<int32_t*>(smem);
+  const bool bt_staged = P.bt_stride <= kPipe / 4;
+  if (bt_staged)
+    for (int i = threadIdx.x; i < P.bt_stride; i += blockDim.x) s_bt[i] = bt_row[i];
   griddep_wait();  // the packed selection (and merge tickets) are written
   int n = prow[Wcols];
   bool bad_row = req < 0;
@@ -150,7 +159,7 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
   const float sl2 = 0.08838834764831845f * kLog2e;  // 128^-0.5 * log2(e)
 
   uint8_t* my = smem + warp * kStages * kSlab;
-  const int32_t* bt_row = P.block_table + static_cast<long long>(req < 0 ? 0 : req) * P.bt_stride;
+  __syncthreads();  // the staged block-table row is complete
 
   // Prologue: KV row id (block * Hkv + kvh) * page + offset of every token of
   // this CTA's range, or kBadRow for a masked entry.
@@ -159,7 +168,7 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     uint32_t rid = kBadRow;
     const int blk = tok >= 0 ? tok / P.page : -1;
     if (tok >= 0 && blk < P.bt_stride) {
-      const int pid = bt_row[blk];
+      const int pid = bt_staged ? s_bt[blk] : bt_row[blk];
       if (pid >= 0 && pid < P.num_blocks)
         rid = static_cast<uint32_t>((static_cast<long long>(pid) * P.hkv + kvh) * P.page +
                                     (tok - blk * P.page));

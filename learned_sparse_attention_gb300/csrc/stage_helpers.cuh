@@ -12,29 +12,49 @@ namespace qsa {
 // Ring commit of one row by 16 lanes: the row's raw key (and 3-D position)
 // goes to ring slot p % S of its request, unless a later row of the same
 // request in this step maps to the same slot.  Must run after every pooling
-// read of the step.
-__device__ __forceinline__ void ring_commit_row(const CompressParams& P, int row, int lane16) {
+// read of the step.  Split in two so that the loads (caller inputs only) can
+// run before a kernel waits on its predecessor and only the store after.
+struct RingCommit {
+  long long slot;  // ring row, or -1 for no write
+  uint4 key;       // this lane's 16 bytes of the raw key
+  long long pos;   // this lane's position component (lanes 0-2, MRoPE)
+};
+
+__device__ __forceinline__ RingCommit ring_commit_prepare(const CompressParams& P, int row,
+                                                          int lane16) {
+  RingCommit rc;
+  rc.slot = -1;
+  rc.pos = 0;
   const int req = P.token_to_req[row];
-  if (req < 0 || req >= P.reqs) return;  // counted by the compress kernel
+  if (req < 0 || req >= P.reqs) return rc;  // counted by the compress kernel
   const int last_row = P.qsl[req + 1] - 1;
   if (last_row < row || last_row >= P.rows) {  // inconsistent query_start_loc
     if (lane16 == 0) flag_error(P.err);
-    return;
+    return rc;
   }
   const int p = P.logical[row];
   const int p_last = P.logical[last_row];
-  if (p + P.S <= p_last) return;  // overwritten later in this step
+  if (p + P.S <= p_last) return rc;  // overwritten later in this step
   const int ring_block = P.ring_bt[static_cast<long long>(req) * P.ring_bt_stride];
   if (ring_block < 0 || ring_block >= P.ring_blocks || p < 0) {
     if (lane16 == 0) flag_error(P.err);
-    return;
+    return rc;
   }
-  const long long ring_slot = static_cast<long long>(ring_block) * P.S + (p % P.S);
-  const uint4 v =
-      *reinterpret_cast<const uint4*>(P.raw_keys + static_cast<long long>(row) * 128 + 8 * lane16);
-  *reinterpret_cast<uint4*>(P.ring + ring_slot * 128 + 8 * lane16) = v;
-  if (P.ring_pos != nullptr && lane16 < 3)
-    P.ring_pos[ring_slot * 3 + lane16] = P.positions[static_cast<long long>(row) * 3 + lane16];
+  rc.slot = static_cast<long long>(ring_block) * P.S + (p % P.S);
+  rc.key = *reinterpret_cast<const uint4*>(P.raw_keys + static_cast<long long>(row) * 128 + 8 * lane16);
+  if (P.ring_pos != nullptr && lane16 < 3) rc.pos = P.positions[static_cast<long long>(row) * 3 + lane16];
+  return rc;
+}
+
+__device__ __forceinline__ void ring_commit_store(const CompressParams& P, const RingCommit& rc,
+                                                  int lane16) {
+  if (rc.slot < 0) return;
+  *reinterpret_cast<uint4*>(P.ring + rc.slot * 128 + 8 * lane16) = rc.key;
+  if (P.ring_pos != nullptr && lane16 < 3) P.ring_pos[rc.slot * 3 + lane16] = rc.pos;
+}
+
+__device__ __forceinline__ void ring_commit_row(const CompressParams& P, int row, int lane16) {
+  ring_commit_store(P, ring_commit_prepare(P, row, lane16), lane16);
 }
 
 // Row group g of the logits kernel, found by the whole block: the rows of

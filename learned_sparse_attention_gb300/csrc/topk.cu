@@ -243,16 +243,25 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
 // ---------------------------------------------------------------------------
 // Register variant for V <= kRegKeys * kRegThreads (16384): thread t owns the
 // kpt consecutive blocks [kpt t, kpt t + kpt) (kpt = V / 512 rounded up to a
-// multiple of 4, at most 32) and keeps their keys in registers, so every
-// thread shares the radix passes whatever V is.
-// Radix passes use per-warp private histograms (no cross-warp contention); the
-// final selection is a per-thread bit mask, so the ordered compaction is one
-// block scan of popcounts, ties going to the lower block by construction.
+// multiple of 4, at most 32) and keeps their keys in registers.
+//  - Everything that reads only caller inputs (the row's position, the
+//    histogram clear) happens before the wait on the logits kernel.
+//  - Radix passes take 11-bit digits below the bits that the row's smallest
+//    and largest keys share, into one 2048-bin shared histogram; a block scan
+//    from the top bin finds the bin holding the K_b-th largest key.  Once
+//    that bin holds at most 32 keys, one warp sorts them (bitonic, in
+//    registers) and reads off the threshold key T and how many keys equal to
+//    T are taken.
+//  - The final selection is a per-thread bit mask; one block scan of
+//    popcounts gives every thread the output slot of its first selected
+//    block (ties go to the lower block by construction), and each thread
+//    writes its selected blocks' tokens straight into the packed row.
 constexpr int kRegThreads = 512;
 constexpr int kRegKeys = 32;
 constexpr int kRegWarps = kRegThreads / 32;
-constexpr int kCand = 2048;     // candidate buffer of the warp-level tail (shared memory)
-constexpr int kCandWarp = 256;  // the tail takes over once the chosen bin holds this few keys
+constexpr int kDigitBits = 11;
+constexpr int kBins = 1 << kDigitBits;  // 2048 = 4 bins per thread
+constexpr int kTail = 32;               // a warp finishes once the chosen bin holds this few keys
 
 __device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -280,18 +289,23 @@ __device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
   return ex;
 }
 
+// KPT: keys per thread the loops are unrolled for (4, 8, 16 or 32), the
+// smallest that covers the launch's max_visible.
+template <int KPT>
 __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams P) {
-  __shared__ int whist[kRegWarps][256];
-  __shared__ int sel[kRegKeys * kRegThreads / 4];  // K_b <= V / ... bounded by token_topk / r
+  __shared__ int hist[kBins];
+  __shared__ uint32_t cand[kTail];
   __shared__ int scratch[32];
   __shared__ uint32_t s_min[kRegWarps], s_max[kRegWarps];
-  __shared__ int s_digit, s_k, s_cnt;
+  __shared__ int s_digit, s_k, s_cnt, s_ncand;
 
   griddep_launch_dependents();
-  if (P.tickets != nullptr && threadIdx.x < P.tickets_per_row)
-    P.tickets[static_cast<long long>(blockIdx.x) * P.tickets_per_row + threadIdx.x] = 0u;
-  griddep_wait();  // logits (and, transitively, the compress kernel) are done
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // caller inputs only, before the wait
+  if (P.tickets != nullptr && tid < P.tickets_per_row)
+    P.tickets[static_cast<long long>(row) * P.tickets_per_row + tid] = 0u;
+  for (int i = tid; i < kBins; i += kRegThreads) hist[i] = 0;
+  if (tid == 0) s_ncand = 0;
   const int r = P.ratio;
   const int kb = P.token_topk / r;
   const int W = P.token_topk + r - 1;
@@ -307,16 +321,29 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
     p = V * r - 1;
   }
   const bool take_all = V <= kb;
+  const int kpt = min(KPT, ((V + kRegThreads - 1) / kRegThreads + 3) & ~3);
+  const int base = tid * kpt;
+  int32_t* prow = P.packed + static_cast<long long>(row) * (W + 1);
+  // Inside the layer step this launch also commits the row's raw key to the
+  // compressor-state ring: its loads (caller inputs) are issued now, the
+  // store after the wait (all pooling reads of the step are done by then).
+  RingCommit rc;
+  rc.slot = -1;
+  if (P.do_ring && tid >= 32 && tid < 48) rc = ring_commit_prepare(P.ring, row, tid - 32);
+  griddep_wait();  // logits (and, transitively, the compress kernel) are done
+  if (P.do_ring && tid >= 32 && tid < 48) ring_commit_store(P.ring, rc, tid - 32);
+
+  const int nsel = take_all ? V : kb;
+  const int tail0 = V * r;
+  const int count = nsel * r + (p + 1 - tail0);
   if (!take_all) {
-    // keys of blocks [kpt tid, kpt tid + kpt); 0 marks "beyond V" (no real
-    // score maps to 0)
-    const int kpt = min(kRegKeys, ((V + kRegThreads - 1) / kRegThreads + 3) & ~3);
-    const int base = tid * kpt;
+    // keys of blocks [base, base + kpt); 0 marks "beyond V" (no real score
+    // maps to 0)
     const float* lrow = P.logits + static_cast<long long>(row) * P.ld;
-    uint32_t key[kRegKeys];
+    uint32_t key[KPT];
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
-    for (int j = 0; j < kRegKeys; j += 4) {
+    for (int j = 0; j < KPT; j += 4) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (j < kpt) {
         if (base + j + 3 < V) v = *reinterpret_cast<const float4*>(lrow + base + j);
@@ -354,6 +381,8 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
       kmin = min(kmin, s_min[w]);
       kmax = max(kmax, s_max[w]);
     }
+    // Bits above the highest bit where the smallest and largest keys differ
+    // are common to every key: the radix passes start below them.
     const uint32_t diff = kmin ^ kmax;
     int hi = diff ? 31 - __clz(diff) : -1;
     uint32_t prefix, pmask;
@@ -369,115 +398,61 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
     }
     int k = kb;
     while (hi >= 0) {
-      const int width = hi + 1 < 8 ? hi + 1 : 8;
+      const int width = hi + 1 < kDigitBits ? hi + 1 : kDigitBits;
       const int shift = hi - width + 1;
       const uint32_t dmask = (1u << width) - 1u;
-      for (int i = lane; i < 256; i += 32) whist[warp][i] = 0;
-      __syncwarp();
 #pragma unroll
-      for (int j = 0; j < kRegKeys; ++j) {
-        if (key[j] != 0u && (key[j] & pmask) == prefix)
-          atomicAdd(&whist[warp][(key[j] >> shift) & dmask], 1);
-      }
+      for (int j = 0; j < KPT; ++j)
+        if (key[j] != 0u && (key[j] & pmask) == prefix) atomicAdd(&hist[(key[j] >> shift) & dmask], 1);
       __syncthreads();
-      if (tid < 256) {
-        int c = 0;
+      // bins from the top: thread t holds bins kBins-1-4t .. kBins-4-4t
+      int c[4], tot = 0;
 #pragma unroll
-        for (int w = 0; w < kRegWarps; ++w) c += whist[w][tid];
-        whist[0][tid] = c;
+      for (int u = 0; u < 4; ++u) {
+        c[u] = hist[kBins - 1 - 4 * tid - u];
+        hist[kBins - 1 - 4 * tid - u] = 0;  // clear for a further pass
+        tot += c[u];
       }
-      __syncthreads();
-      if (warp == 0) {
-        int cnt[8], tot = 0;
+      int total;
+      int cum = block_sum_excl(tot, scratch, &total);  // keys in higher bins
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          cnt[j] = whist[0][255 - 8 * lane - j];
-          tot += cnt[j];
+      for (int u = 0; u < 4; ++u) {
+        if (cum < k && k <= cum + c[u]) {
+          s_digit = kBins - 1 - 4 * tid - u;
+          s_k = k - cum;
+          s_cnt = c[u];
         }
-        int incl = tot;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += y;
-        }
-        int cum = incl - tot;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (cum < k && k <= cum + cnt[j]) {
-            s_digit = 255 - 8 * lane - j;
-            s_k = k - cum;
-            s_cnt = cnt[j];
-          }
-          cum += cnt[j];
-        }
+        cum += c[u];
       }
       __syncthreads();
       prefix |= static_cast<uint32_t>(s_digit) << shift;
       pmask |= dmask << shift;
       k = s_k;
       hi = shift - 1;
-      if (hi >= 0 && s_cnt <= kCandWarp) {
-        // Few keys left in the chosen bin: gather them and let warp 0 finish
-        // the radix select with warp-level syncs only.
-        int mine = 0;
+      const int cnt = s_cnt;
+      if (hi >= 0 && cnt <= kTail) {
+        // The chosen bin holds at most 32 keys: gather them, and one warp
+        // sorts them in descending order (bitonic network over the lanes).
 #pragma unroll
-        for (int j = 0; j < kRegKeys; ++j) mine += (key[j] != 0u && (key[j] & pmask) == prefix) ? 1 : 0;
-        int ncand;
-        int at = block_sum_excl(mine, scratch, &ncand);
-        uint32_t* cand = reinterpret_cast<uint32_t*>(&whist[0][0]);    // kCand keys
-        int* h = &whist[kCand / 256][0];                                // 256 bins
-#pragma unroll
-        for (int j = 0; j < kRegKeys; ++j)
-          if (key[j] != 0u && (key[j] & pmask) == prefix) cand[at++] = key[j];
+        for (int j = 0; j < KPT; ++j)
+          if (key[j] != 0u && (key[j] & pmask) == prefix) cand[atomicAdd(&s_ncand, 1)] = key[j];
         __syncthreads();
         if (warp == 0) {
-          while (hi >= 0) {
-            const int width = hi + 1 < 8 ? hi + 1 : 8;
-            const int shift = hi - width + 1;
-            const uint32_t dmask = (1u << width) - 1u;
+          uint32_t v = lane < cnt ? cand[lane] : 0u;
 #pragma unroll
-            for (int i = lane; i < 256; i += 32) h[i] = 0;
-            __syncwarp();
-            for (int i = lane; i < ncand; i += 32) {
-              const uint32_t c = cand[i];
-              if ((c & pmask) == prefix) atomicAdd(&h[(c >> shift) & dmask], 1);
-            }
-            __syncwarp();
-            int cnt[8], tot = 0;
+          for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              cnt[j] = h[255 - 8 * lane - j];
-              tot += cnt[j];
+            for (int stride = size / 2; stride > 0; stride >>= 1) {
+              const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+              const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+              v = keep_max ? max(v, o) : min(v, o);
             }
-            int incl = tot;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-              const int y = __shfl_up_sync(0xffffffffu, incl, off);
-              if (lane >= off) incl += y;
-            }
-            int cum = incl - tot, digit = 0, knew = 0, found = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (cum < k && k <= cum + cnt[j]) {
-                digit = 255 - 8 * lane - j;
-                knew = k - cum;
-                found = 1;
-              }
-              cum += cnt[j];
-            }
-            const unsigned who = __ballot_sync(0xffffffffu, found);
-            const int src = who ? __ffs(who) - 1 : 0;
-            digit = __shfl_sync(0xffffffffu, digit, src);
-            knew = __shfl_sync(0xffffffffu, knew, src);
-            prefix |= static_cast<uint32_t>(digit) << shift;
-            pmask |= dmask << shift;
-            k = knew;
-            hi = shift - 1;
-            __syncwarp();
           }
+          const uint32_t t = __shfl_sync(0xffffffffu, v, k - 1);  // k-th largest of the bin
+          const int above = __popc(__ballot_sync(0xffffffffu, v > t));
           if (lane == 0) {
-            s_digit = static_cast<int>(prefix);
-            s_k = k;
+            s_digit = static_cast<int>(t);
+            s_k = k - above;
           }
         }
         __syncthreads();
@@ -490,12 +465,12 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
     const int keq = k;
     uint32_t gt_mask = 0u, eq_mask = 0u;
 #pragma unroll
-    for (int j = 0; j < kRegKeys; ++j) {
+    for (int j = 0; j < KPT; ++j) {
       gt_mask |= (key[j] > T ? 1u : 0u) << j;
       eq_mask |= (key[j] == T ? 1u : 0u) << j;
     }
-    // one scan of (greater, equal) counts: every greater key is taken and the
-    // first keq equal keys in block order
+    // one scan of (greater, equal) counts: every greater key is taken and
+    // the first keq equal keys in block order
     int tot;
     const int both = block_sum_excl((__popc(gt_mask) << 16) | __popc(eq_mask), scratch, &tot);
     const int gt_before = both >> 16, eq_before = both & 0xFFFF;
@@ -507,28 +482,24 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
     int out = gt_before + (eq_before < keq ? eq_before : keq);
     while (m) {
       const int j = __ffs(m) - 1;
-      sel[out++] = base + j;
+      const int b = base + j;
+      int32_t* dst = prow + out * r;
+      for (int t = 0; t < r; ++t) dst[t] = b * r + t;
+      ++out;
       m &= m - 1u;
     }
-    __syncthreads();
-  }
-
-  const int nsel = take_all ? V : kb;
-  const int tail0 = V * r;
-  const int count = nsel * r + (p + 1 - tail0);
-  int32_t* prow = P.packed + static_cast<long long>(row) * (W + 1);
-  for (int idx = tid; idx < W; idx += kRegThreads) {
-    int v = -1;
-    if (idx < nsel * r) {
-      const int b = take_all ? idx / r : sel[idx / r];
-      v = b * r + idx % r;
-    } else if (idx < count) {
-      v = tail0 + (idx - nsel * r);
+    // the tail tokens of the open group, then -1 padding
+    for (int idx = nsel * r + tid; idx < W; idx += kRegThreads)
+      prow[idx] = idx < count ? tail0 + (idx - nsel * r) : -1;
+  } else {
+    for (int idx = tid; idx < W; idx += kRegThreads) {
+      int v = -1;
+      if (idx < nsel * r) v = idx;  // block idx / r, token idx % r
+      else if (idx < count) v = tail0 + (idx - nsel * r);
+      prow[idx] = v;
     }
-    prow[idx] = v;
   }
   if (tid == 0) prow[W] = count;
-  if (P.do_ring && tid >= 32 && tid < 48) ring_commit_row(P.ring, row, tid - 32);
 }
 
 }  // namespace
@@ -539,8 +510,13 @@ size_t topk_smem_bytes(int max_visible, int block_topk) {
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
-  if (p.max_visible <= kRegKeys * kRegThreads && p.token_topk / p.ratio <= kRegKeys * kRegThreads / 4)
-    return launch_kernel(topk_reg_kernel, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+  if (p.max_visible <= kRegKeys * kRegThreads && p.token_topk / p.ratio <= kRegKeys * kRegThreads / 4) {
+    const int kpt = (p.max_visible + kRegThreads - 1) / kRegThreads;
+    if (kpt <= 4) return launch_kernel(topk_reg_kernel<4>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+    if (kpt <= 8) return launch_kernel(topk_reg_kernel<8>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+    if (kpt <= 16) return launch_kernel(topk_reg_kernel<16>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+    return launch_kernel(topk_reg_kernel<32>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+  }
   const size_t smem = topk_smem_bytes(p.max_visible, p.token_topk / p.ratio);
   cudaError_t e =
       cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
