@@ -66,6 +66,19 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int elem_bytes, long lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Multiprocessors of the current device (queried once per device).
+int sm_count() {
+  static int count[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+  if (count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    count[dev] = n;
+  }
+  return count[dev];
+}
+
 bool pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -260,9 +273,16 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
   if (p.err == nullptr) return QSA_ERR_CUDA;
 
   const int max_tiles = (max_visible + 127) / 128;
-  // Spread the key tiles so that about four CTAs per SM are available.
-  const long long work = static_cast<long long>(max_groups) * max_tiles;
-  long long tpc = (work + 4 * 152 - 1) / (4 * 152);
+  // Split each row group's key tiles into chunks so that the CTAs with work
+  // (about ceil(rows / (R * G)) groups x chunks) fill one wave: 4 CTAs per SM
+  // for the narrow kernels (N <= 64), 1 for the wide ones (their shared
+  // memory and 256-512 TMEM columns).  The grid also holds the groups that a
+  // ragged batch may need beyond that estimate; those CTAs leave at once.
+  const long long slots = static_cast<long long>(sm_count()) * (npad <= 64 ? 4 : 1);
+  const long long groups_est = (rows + static_cast<long long>(R) * G - 1) / (static_cast<long long>(R) * G);
+  long long chunks_target = slots / (groups_est > 0 ? groups_est : 1);
+  if (chunks_target < 1) chunks_target = 1;
+  long long tpc = (max_tiles + chunks_target - 1) / chunks_target;
   if (tpc < 2) tpc = 2;
   if (tpc > max_tiles) tpc = max_tiles;
   if (tpc * (128 / cfg->cpage) > 4096) tpc = 4096 / (128 / cfg->cpage);

@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     if (lane == 0) s_vmask[warp][stage] = vm;
     uint8_t* dst_base = my + stage * kSlab;
     const int chunk = lane & 15, is_v = lane >> 4;
-#pragma unroll 4
+#pragma unroll
     for (int j = 0; j < 16; ++j) {
       const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
       const bool okj = (vm >> j) & 1u;
@@ -207,15 +207,22 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     const uint8_t* sK = my + stage * kSlab;
     const uint8_t* sV = sK + 4096;
 
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // S^T = K.Q^T over 8 K-steps, split over two accumulators so that the
+    // MMAs form two dependent chains of four instead of one of eight
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       uint32_t a[4];
       const int rl = lane & 15;
       const int ch = 2 * kk + (lane >> 4);
       ldmatrix_x4(a, sK + rl * 256 + ((ch ^ (rl & 7)) << 4));
-      mma_bf16_16816(s, a, qb[kk][0], qb[kk][1]);
+      if (kk & 1)
+        mma_bf16_16816(s2, a, qb[kk][0], qb[kk][1]);
+      else
+        mma_bf16_16816(s, a, qb[kk][0], qb[kk][1]);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[e] += s2[e];
     const uint32_t vm = s_vmask[warp][stage];
     const bool v0 = (vm >> g) & 1u, v1 = (vm >> (g + 8)) & 1u;
     const float x0 = v0 ? s[0] * sl2 : -INFINITY;  // token g,   head 2t
@@ -236,15 +243,19 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
     l0 = l0 * al0 + p0 + p2;
     l1 = l1 * al1 + p1 + p3;
+    // the accumulator needs rescaling only where a running max grew (the
+    // factor is exactly 1 elsewhere): skipped when no lane's max moved
+    if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
     m0 = mn0;
     m1 = mn1;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
-    }
     const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
     const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
 #pragma unroll
