@@ -274,16 +274,17 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
 
   const int max_tiles = (max_visible + 127) / 128;
   // Split each row group's key tiles into chunks so that the CTAs with work
-  // (about ceil(rows / (R * G)) groups x chunks) fill one wave: 4 CTAs per SM
-  // for the narrow kernels (N <= 64), 1 for the wide ones (their shared
-  // memory and 256-512 TMEM columns).  The grid also holds the groups that a
+  // (about ceil(rows / (R * G)) groups x chunks) fill one wave: 3 CTAs per SM
+  // for the narrow kernels (N <= 64; 4 fit, but the compress kernel's CTAs
+  // still hold registers on some SMs when they start: measured faster), 1 for
+  // the wide ones (their shared memory and 256-512 TMEM columns).  The grid also holds the groups that a
   // ragged batch may need beyond that estimate; those CTAs leave at once.
-  const long long slots = static_cast<long long>(sm_count()) * (npad <= 64 ? 4 : 1);
+  const long long slots = static_cast<long long>(sm_count()) * (npad <= 64 ? 3 : 1);
   const long long groups_est = (rows + static_cast<long long>(R) * G - 1) / (static_cast<long long>(R) * G);
   long long chunks_target = slots / (groups_est > 0 ? groups_est : 1);
   if (chunks_target < 1) chunks_target = 1;
   long long tpc = (max_tiles + chunks_target - 1) / chunks_target;
-  if (tpc < 2) tpc = 2;
+  if (tpc < 4) tpc = 4;  // amortise each CTA's set-up (measured on the long-context decode)
   if (tpc > max_tiles) tpc = max_tiles;
   if (tpc * (128 / cfg->cpage) > 4096) tpc = 4096 / (128 / cfg->cpage);
   p.tiles_per_cta = static_cast<int>(tpc);

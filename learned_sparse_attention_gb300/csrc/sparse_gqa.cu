@@ -207,22 +207,22 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     const uint8_t* sK = my + stage * kSlab;
     const uint8_t* sV = sK + 4096;
 
-    // S^T = K.Q^T over 8 K-steps, split over two accumulators so that the
-    // MMAs form two dependent chains of four instead of one of eight
-    float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+    // S^T = K.Q^T over 8 K-steps, split over four accumulators so that the
+    // MMAs form four dependent chains of two instead of one of eight
+    float sa[4][4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) sa[c][0] = sa[c][1] = sa[c][2] = sa[c][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       uint32_t a[4];
       const int rl = lane & 15;
       const int ch = 2 * kk + (lane >> 4);
       ldmatrix_x4(a, sK + rl * 256 + ((ch ^ (rl & 7)) << 4));
-      if (kk & 1)
-        mma_bf16_16816(s2, a, qb[kk][0], qb[kk][1]);
-      else
-        mma_bf16_16816(s, a, qb[kk][0], qb[kk][1]);
+      mma_bf16_16816(sa[kk & 3], a, qb[kk][0], qb[kk][1]);
     }
+    float s[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[e] += s2[e];
+    for (int e = 0; e < 4; ++e) s[e] = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
     const uint32_t vm = s_vmask[warp][stage];
     const bool v0 = (vm >> g) & 1u, v1 = (vm >> (g + 8)) & 1u;
     const float x0 = v0 ? s[0] * sl2 : -INFINITY;  // token g,   head 2t
@@ -238,14 +238,15 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
     const float b0 = mn0 == -INFINITY ? 0.f : mn0;
     const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = exp2f(m0 - b0), al1 = exp2f(m1 - b1);
     const float p0 = exp2f(x0 - b0), p1 = exp2f(x1 - b1);
     const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
-    l0 = l0 * al0 + p0 + p2;
-    l1 = l1 * al1 + p1 + p3;
-    // the accumulator needs rescaling only where a running max grew (the
-    // factor is exactly 1 elsewhere): skipped when no lane's max moved
+    // the running sums and the accumulator need rescaling only where a
+    // running max grew (the factor is exactly 1 elsewhere): skipped when no
+    // lane's max moved
     if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+      const float al0 = exp2f(m0 - b0), al1 = exp2f(m1 - b1);
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         o[mt][0] *= al0;
@@ -254,6 +255,8 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
         o[mt][3] *= al1;
       }
     }
+    l0 += p0 + p2;
+    l1 += p1 + p3;
     m0 = mn0;
     m1 = mn1;
     const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
