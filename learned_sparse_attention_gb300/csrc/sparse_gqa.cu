@@ -360,7 +360,10 @@ int gqa_num_splits(int rows, int hkv, int packed_width) {
   if (base <= 0) return 1;
   const int max_tiles = (packed_width - 1 + kTile - 1) / kTile;
   const int min_s = (max_tiles + kMaxTiles - 1) / kMaxTiles;
-  long long s = (152 + base - 1) / base;
+  // as many splits as keep every (row, KV head, split) CTA resident in one
+  // wave at two CTAs per SM (shared memory): a CTA's time grows with its
+  // tokens, so shorter splits finish the launch sooner
+  long long s = 2 * 152 / base;
   if (s > max_tiles) s = max_tiles;
   if (s > 64) s = 64;
   if (s < min_s) s = min_s;

@@ -256,13 +256,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams P) {
 //    popcounts gives every thread the output slot of its first selected
 //    block (ties go to the lower block by construction), and each thread
 //    writes its selected blocks' tokens straight into the packed row.
-constexpr int kRegThreads = 512;
+constexpr int kRegThreads = 512;   // the launch width for many rows (two CTAs per SM)
 constexpr int kRegKeys = 32;
-constexpr int kRegWarps = kRegThreads / 32;
 constexpr int kDigitBits = 11;
 constexpr int kBins = 1 << kDigitBits;  // 2048 = 4 bins per thread
 constexpr int kTail = 32;               // a warp finishes once the chosen bin holds this few keys
 
+template <int NWARPS>
 __device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -274,29 +274,31 @@ __device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
   if (lane == 31) scratch[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int x = lane < kRegWarps ? scratch[lane] : 0;
+    int x = lane < NWARPS ? scratch[lane] : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, x, off);
       if (lane >= off) x += y;
     }
-    if (lane < kRegWarps) scratch[lane] = x;
+    if (lane < NWARPS) scratch[lane] = x;
   }
   __syncthreads();
   const int ex = (warp > 0 ? scratch[warp - 1] : 0) + incl - v;
-  *total = scratch[kRegWarps - 1];
+  *total = scratch[NWARPS - 1];
   __syncthreads();
   return ex;
 }
 
 // KPT: keys per thread the loops are unrolled for (4, 8, 16 or 32), the
-// smallest that covers the launch's max_visible.
-template <int KPT>
-__global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams P) {
+// smallest that covers the launch's max_visible with NT threads (512, or 1024
+// when there are fewer rows than half the SMs).
+template <int KPT, int NT>
+__global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const TopkParams P) {
+  constexpr int NW = NT / 32;
   __shared__ int hist[kBins];
   __shared__ uint32_t cand[kTail];
   __shared__ int scratch[32];
-  __shared__ uint32_t s_min[kRegWarps], s_max[kRegWarps];
+  __shared__ uint32_t s_min[NW], s_max[NW];
   __shared__ int s_digit, s_k, s_cnt, s_ncand;
 
   griddep_launch_dependents();
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
   // caller inputs only, before the wait
   if (P.tickets != nullptr && tid < P.tickets_per_row)
     P.tickets[static_cast<long long>(row) * P.tickets_per_row + tid] = 0u;
-  for (int i = tid; i < kBins; i += kRegThreads) hist[i] = 0;
+  for (int i = tid; i < kBins; i += NT) hist[i] = 0;
   if (tid == 0) s_ncand = 0;
   const int r = P.ratio;
   const int kb = P.token_topk / r;
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
     p = V * r - 1;
   }
   const bool take_all = V <= kb;
-  const int kpt = min(KPT, ((V + kRegThreads - 1) / kRegThreads + 3) & ~3);
+  const int kpt = min(KPT, ((V + NT - 1) / NT + 3) & ~3);
   const int base = tid * kpt;
   int32_t* prow = P.packed + static_cast<long long>(row) * (W + 1);
   // Inside the layer step this launch also commits the row's raw key to the
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
     kmin = 0xFFFFFFFFu;
     kmax = 0u;
 #pragma unroll
-    for (int w = 0; w < kRegWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       kmin = min(kmin, s_min[w]);
       kmax = max(kmax, s_max[w]);
     }
@@ -405,20 +407,21 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
       for (int j = 0; j < KPT; ++j)
         if (key[j] != 0u && (key[j] & pmask) == prefix) atomicAdd(&hist[(key[j] >> shift) & dmask], 1);
       __syncthreads();
-      // bins from the top: thread t holds bins kBins-1-4t .. kBins-4-4t
-      int c[4], tot = 0;
+      // bins from the top: thread t holds BPT consecutive bins
+      constexpr int BPT = kBins / NT;
+      int c[BPT], tot = 0;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        c[u] = hist[kBins - 1 - 4 * tid - u];
-        hist[kBins - 1 - 4 * tid - u] = 0;  // clear for a further pass
+      for (int u = 0; u < BPT; ++u) {
+        c[u] = hist[kBins - 1 - BPT * tid - u];
+        hist[kBins - 1 - BPT * tid - u] = 0;  // clear for a further pass
         tot += c[u];
       }
       int total;
-      int cum = block_sum_excl(tot, scratch, &total);  // keys in higher bins
+      int cum = block_sum_excl<NW>(tot, scratch, &total);  // keys in higher bins
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < BPT; ++u) {
         if (cum < k && k <= cum + c[u]) {
-          s_digit = kBins - 1 - 4 * tid - u;
+          s_digit = kBins - 1 - BPT * tid - u;
           s_k = k - cum;
           s_cnt = c[u];
         }
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
     // one scan of (greater, equal) counts: every greater key is taken and
     // the first keq equal keys in block order
     int tot;
-    const int both = block_sum_excl((__popc(gt_mask) << 16) | __popc(eq_mask), scratch, &tot);
+    const int both = block_sum_excl<NW>((__popc(gt_mask) << 16) | __popc(eq_mask), scratch, &tot);
     const int gt_before = both >> 16, eq_before = both & 0xFFFF;
     int take = keq - eq_before;
     take = take < 0 ? 0 : take;
@@ -489,10 +492,10 @@ __global__ void __launch_bounds__(kRegThreads) topk_reg_kernel(const TopkParams 
       m &= m - 1u;
     }
     // the tail tokens of the open group, then -1 padding
-    for (int idx = nsel * r + tid; idx < W; idx += kRegThreads)
+    for (int idx = nsel * r + tid; idx < W; idx += NT)
       prow[idx] = idx < count ? tail0 + (idx - nsel * r) : -1;
   } else {
-    for (int idx = tid; idx < W; idx += kRegThreads) {
+    for (int idx = tid; idx < W; idx += NT) {
       int v = -1;
       if (idx < nsel * r) v = idx;  // block idx / r, token idx % r
       else if (idx < count) v = tail0 + (idx - nsel * r);
@@ -511,11 +514,17 @@ size_t topk_smem_bytes(int max_visible, int block_topk) {
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
   if (p.max_visible <= kRegKeys * kRegThreads && p.token_topk / p.ratio <= kRegKeys * kRegThreads / 4) {
+    // few rows: twice the threads per row, half the keys per thread
+    if (p.rows < 76 && p.max_visible > 4 * 1024) {
+      const int kpt = (p.max_visible + 1023) / 1024;
+      if (kpt <= 8) return launch_kernel(topk_reg_kernel<8, 1024>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
+      return launch_kernel(topk_reg_kernel<16, 1024>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
+    }
     const int kpt = (p.max_visible + kRegThreads - 1) / kRegThreads;
-    if (kpt <= 4) return launch_kernel(topk_reg_kernel<4>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
-    if (kpt <= 8) return launch_kernel(topk_reg_kernel<8>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
-    if (kpt <= 16) return launch_kernel(topk_reg_kernel<16>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
-    return launch_kernel(topk_reg_kernel<32>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+    if (kpt <= 4) return launch_kernel(topk_reg_kernel<4, kRegThreads>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+    if (kpt <= 8) return launch_kernel(topk_reg_kernel<8, kRegThreads>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+    if (kpt <= 16) return launch_kernel(topk_reg_kernel<16, kRegThreads>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+    return launch_kernel(topk_reg_kernel<32, kRegThreads>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
   }
   const size_t smem = topk_smem_bytes(p.max_visible, p.token_topk / p.ratio);
   cudaError_t e =
