@@ -192,7 +192,8 @@ qsa_status qsa_topk(const qsa_cfg* cfg, const float* logits, int64_t ld,
  *         block_table[q, t / page_size], offset t % page_size
  *  packed [rows, packed_width] int32; token_to_req [rows]
  *  gate   [rows, Hq, D] bf16 or NULL;  out [rows, Hq, D] bf16
- *  ws     scratch (split-KV partials), qsa_workspace_bytes() bytes
+ *  ws     scratch (split-KV partials and their merge tickets),
+ *         qsa_workspace_bytes() bytes
  */
 qsa_status qsa_sparse_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
                           const int32_t* block_table, int32_t bt_stride,

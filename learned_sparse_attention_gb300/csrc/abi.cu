@@ -138,13 +138,26 @@ long long logits_ld(int max_visible) { return (static_cast<long long>(max_visibl
 // The logits kernel needs no scratch (each CTA finds its own row group).
 size_t logits_ws_bytes(int, int, const qsa_cfg*) { return 0; }
 
+// GQA scratch: fp32 partial slots, their log-sum-exps and the merge tickets.
+struct GqaLayout {
+  int splits;
+  size_t po, pl, tickets, total;  // byte offsets of the regions, total size
+};
+
+GqaLayout gqa_layout(const qsa_gqa_cfg* g, int rows, int packed_width) {
+  GqaLayout L{};
+  L.splits = gqa_num_splits(rows, g->num_kv_heads, packed_width);
+  if (L.splits == 1) return L;
+  const long long slots = static_cast<long long>(L.splits) * rows * g->num_kv_heads;
+  L.po = 0;
+  L.pl = align256(static_cast<size_t>(slots) * 8 * 128 * sizeof(float));
+  L.tickets = L.pl + align256(static_cast<size_t>(slots) * 8 * sizeof(float));
+  L.total = L.tickets + align256(static_cast<size_t>(rows) * g->num_kv_heads * sizeof(unsigned));
+  return L;
+}
+
 size_t gqa_ws_bytes(const qsa_gqa_cfg* g, int rows, int packed_width) {
-  const int s = gqa_num_splits(rows, g->num_kv_heads, packed_width);
-  if (s == 1) return 0;
-  const size_t po = static_cast<size_t>(s) * rows * g->num_q_heads * 128 * sizeof(float);
-  const size_t pl = static_cast<size_t>(s) * rows * g->num_q_heads * sizeof(float);
-  const size_t tickets = static_cast<size_t>(rows) * g->num_kv_heads * sizeof(unsigned);
-  return align256(po) + align256(pl) + align256(tickets);
+  return gqa_layout(g, rows, packed_width).total;
 }
 
 qsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA; }
@@ -387,15 +400,15 @@ qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
   p.hkv = gcfg->num_kv_heads;
   p.page = gcfg->page_size;
   p.num_blocks = gcfg->num_blocks;
-  p.splits = gqa_num_splits(rows, gcfg->num_kv_heads, packed_width);
-  if (p.splits > 1) {
+  const GqaLayout G = gqa_layout(gcfg, rows, packed_width);
+  p.splits = G.splits;
+  if (G.total > 0) {
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255)) return QSA_ERR_WORKSPACE;
-    if (ws_bytes < gqa_ws_bytes(gcfg, rows, packed_width)) return QSA_ERR_WORKSPACE;
-    const size_t po = static_cast<size_t>(p.splits) * rows * p.hq * 128 * sizeof(float);
-    const size_t pl = static_cast<size_t>(p.splits) * rows * p.hq * sizeof(float);
-    p.part_o = static_cast<float*>(ws);
-    p.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(po));
-    p.counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + align256(po) + align256(pl));
+    if (ws_bytes < G.total) return QSA_ERR_WORKSPACE;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    p.part_o = reinterpret_cast<float*>(w + G.po);
+    p.part_lse = reinterpret_cast<float*>(w + G.pl);
+    p.counters = reinterpret_cast<unsigned*>(w + G.tickets);
   }
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
@@ -496,7 +509,7 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int pw = cfg->token_topk + cfg->compress_ratio;
-  const int splits = gqa_num_splits(a->rows, gcfg->num_kv_heads, pw);
+  const GqaLayout G = gqa_layout(gcfg, a->rows, pw);
   // Kernels after the first start early (programmatic dependent launch) and
   // wait on the device for their predecessor's results.
   if (skip_topk) {
@@ -535,12 +548,8 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
   }
   // stage 3; the same launch commits the ring after every pooling read and
   // clears the split-merge tickets of stage 4
-  unsigned* tickets = nullptr;
-  if (splits > 1) {
-    const size_t po = static_cast<size_t>(splits) * a->rows * gcfg->num_q_heads * 128 * sizeof(float);
-    const size_t pl = static_cast<size_t>(splits) * a->rows * gcfg->num_q_heads * sizeof(float);
-    tickets = reinterpret_cast<unsigned*>(w + L.gqa_ws + align256(po) + align256(pl));
-  }
+  unsigned* tickets =
+      G.total > 0 ? reinterpret_cast<unsigned*>(w + L.gqa_ws + G.tickets) : nullptr;
   st = do_topk(cfg, logits, L.ld, a->max_visible, a->logical_positions, a->packed, a->rows, s, &cp,
                tickets, tickets ? gcfg->num_kv_heads : 0, /*pdl=*/any_visible);
   if (st != QSA_OK) return st;
@@ -560,9 +569,7 @@ int32_t qsa_step_launches(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t r
                           int32_t reqs, int32_t skip_topk) {
   if (check_cfg(cfg) != QSA_OK || check_gcfg(gcfg) != QSA_OK || rows < 0 || reqs < 0) return 0;
   if (rows == 0) return 0;
-  const int pw = cfg->token_topk + cfg->compress_ratio;
-  const int splits = gqa_num_splits(rows, gcfg->num_kv_heads, pw);
-  (void)splits;  // split-KV partials are merged inside the GQA kernel
+  // split-KV partials are merged inside the GQA kernel
   return skip_topk ? 3 : 4;
 }
 

@@ -36,6 +36,9 @@ namespace {
 
 constexpr int kG = 8;          // query heads per KV head
 constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRidBatch = 8;  // KV row ids resolved per thread per batch
+constexpr int kFirst = 20;    // packed entries per thread loaded right after the wait
 constexpr int kTile = 64;      // tokens per CTA tile (16 per warp)
 constexpr int kStages = 3;
 constexpr int kSlab = 16 * 512;  // bytes per warp stage: 16 tokens x (K|V)
@@ -48,16 +51,16 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
 
-__device__ __forceinline__ void load_gate8(const uint16_t* gate, long long obase, float (&gv)[8]) {
-  const uint4 gr = *reinterpret_cast<const uint4*>(gate + obase);
-  gv[0] = bf16_lo(gr.x); gv[1] = bf16_hi(gr.x); gv[2] = bf16_lo(gr.y); gv[3] = bf16_hi(gr.y);
-  gv[4] = bf16_lo(gr.z); gv[5] = bf16_hi(gr.z); gv[6] = bf16_lo(gr.w); gv[7] = bf16_hi(gr.w);
+// The gate of 8 dims (bf16x8), or zeros when there is none.
+__device__ __forceinline__ uint4 load_gate8(const GqaParams& P, long long obase) {
+  return P.gate != nullptr ? *reinterpret_cast<const uint4*>(P.gate + obase) : make_uint4(0, 0, 0, 0);
 }
 
 // out[8 dims] = bf16(bf16(x) * sigmoid(gate)) (or bf16(x) without a gate).
-__device__ __forceinline__ void store_out8(const GqaParams& P, long long obase, const float (&x)[8]) {
-  float gv[8];
-  if (P.gate != nullptr) load_gate8(P.gate, obase, gv);
+__device__ __forceinline__ void store_out8(const GqaParams& P, long long obase, const float (&x)[8],
+                                           uint4 gr) {
+  const float gv[8] = {bf16_lo(gr.x), bf16_hi(gr.x), bf16_lo(gr.y), bf16_hi(gr.y),
+                       bf16_lo(gr.z), bf16_hi(gr.z), bf16_lo(gr.w), bf16_hi(gr.w)};
   float y[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -73,7 +76,7 @@ __device__ __forceinline__ void store_out8(const GqaParams& P, long long obase, 
 }
 
 // Log-sum-exp merge of the split partials of 8 dims of one (row, head).
-__device__ __forceinline__ void merge8(const GqaParams& P, int row, int hq, int d0) {
+__device__ __forceinline__ void merge8(const GqaParams& P, int row, int hq, int d0, uint4 gr) {
   float M = -INFINITY;
   for (int s = 0; s < P.splits; ++s)
     M = fmaxf(M, __ldcg(P.part_lse + (static_cast<long long>(s) * P.rows + row) * P.hq + hq));
@@ -92,10 +95,18 @@ __device__ __forceinline__ void merge8(const GqaParams& P, int row, int hq, int 
   const float inv = W > 0.f ? 1.0f / W : 0.f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] *= inv;
-  store_out8(P, (static_cast<long long>(row) * P.hq + hq) * 128 + d0, acc);
+  store_out8(P, (static_cast<long long>(row) * P.hq + hq) * 128 + d0, acc, gr);
 }
 
-__global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
+// KV row id (block * Hkv + kvh) * page + offset of a selected token, or
+// kBadRow for a masked entry (a block id outside the cache).  The host
+// rejects caches whose row ids would not fit 32 bits.
+__device__ __forceinline__ uint32_t kv_row_id(const GqaParams& P, int off, int pid, int kvh) {
+  if (pid < 0 || pid >= P.num_blocks) return kBadRow;
+  return (static_cast<uint32_t>(pid) * P.hkv + kvh) * static_cast<uint32_t>(P.page) + off;
+}
+
+__global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_vmask[kWarps][kStages];
   __shared__ int s_last;
@@ -119,16 +130,40 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     qb[kk][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t);
     qb[kk][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t);
   }
-  // The request's block-table row (a caller input) goes to the pipeline
-  // buffers before the wait, so that resolving the selected tokens' pages
-  // after it costs shared-memory reads instead of a second round trip to
-  // global memory.  Rows longer than the buffers read the table directly.
+  // The request's block-table row (a caller input) is copied before the
+  // wait into the last pipeline stage of all warps (contiguous, and not
+  // written before the main loop), so that resolving the selected tokens'
+  // pages after the wait costs shared-memory reads.  Longer rows, and
+  // token ranges of more than one chunk, read the table in global memory.
   const int32_t* bt_row = P.block_table + static_cast<long long>(req < 0 ? 0 : req) * P.bt_stride;
-  int32_t* s_bt = reinterpret_cast<int32_t*>(smem);
-  const bool bt_staged = P.bt_stride <= kPipe / 4;
-  if (bt_staged)
-    for (int i = threadIdx.x; i < P.bt_stride; i += blockDim.x) s_bt[i] = bt_row[i];
+  int32_t* s_bt = reinterpret_cast<int32_t*>(smem + (kStages - 1) * kWarps * kSlab);
+  const bool bt_fits = P.bt_stride <= kWarps * kSlab / 4;
+  if (bt_fits) {
+    for (int i0 = threadIdx.x; i0 < P.bt_stride; i0 += 8 * kThreads) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = i0 + u * kThreads < P.bt_stride ? bt_row[i0 + u * kThreads] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * kThreads < P.bt_stride) s_bt[i0 + u * kThreads] = v[u];
+    }
+  }
+  // the epilogue's (head, 8 dims) of this thread and their gate (a caller input)
+  const int h = threadIdx.x >> 4;          // 0..7
+  const int d0 = (threadIdx.x & 15) * 8;   // 8 dims per thread
+  const int hq = kvh * kG + h;
+  const long long obase = (static_cast<long long>(row) * P.hq + hq) * 128 + d0;
+  const uint4 gate8 = load_gate8(P, obase);
   griddep_wait();  // the packed selection (and merge tickets) are written
+  // Without split-KV the CTA's range starts at token 0 whatever the count,
+  // so its first entries (kFirst per thread, up to kFirst * kThreads tokens)
+  // load together with the count: one round trip before the first copies.
+  int tk[kFirst];
+#pragma unroll
+  for (int u = 0; u < kFirst; ++u) {
+    const int i = threadIdx.x + u * kThreads;
+    tk[u] = (P.splits == 1 && i < Wcols) ? prow[i] : -1;
+  }
   int n = prow[Wcols];
   bool bad_row = req < 0;
   if (n < 0 || n > Wcols) {
@@ -143,138 +178,173 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
   const int tps = (ntiles + P.splits - 1) / P.splits;
   const int tb = split * tps;
   const int te = min(ntiles, tb + tps);
-  const int nt = max(0, te - tb);
   const int tok0 = tb * kTile;
-  int ntok = nt > 0 ? min(te * kTile, n) - tok0 : 0;
-  if (ntok > kMaxTok) {  // excluded by gqa_num_splits; never read past the stage
-    if (threadIdx.x == 0) flag_error(P.err);
-    ntok = kMaxTok;
-  }
-
+  const int ntok = te > tb ? min(te * kTile, n) - tok0 : 0;
+  const int32_t* ptok = prow + tok0;
+  const bool sbt = bt_fits && ntok <= kMaxTok;
+  __syncthreads();  // the staged block-table row is complete
 
   float o[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const float sl2 = 0.08838834764831845f * kLog2e;  // 128^-0.5 * log2(e)
+  bool bad = false;
 
-  uint8_t* my = smem + warp * kStages * kSlab;
-  __syncthreads();  // the staged block-table row is complete
-
-  // Prologue: KV row id (block * Hkv + kvh) * page + offset of every token of
-  // this CTA's range, or kBadRow for a masked entry.
-  for (int i = threadIdx.x; i < ntok; i += blockDim.x) {
-    const int tok = prow[tok0 + i];
-    uint32_t rid = kBadRow;
-    const int blk = tok >= 0 ? tok / P.page : -1;
-    if (tok >= 0 && blk < P.bt_stride) {
-      const int pid = bt_staged ? s_bt[blk] : bt_row[blk];
-      if (pid >= 0 && pid < P.num_blocks)
-        rid = static_cast<uint32_t>((static_cast<long long>(pid) * P.hkv + kvh) * P.page +
-                                    (tok - blk * P.page));
-    }
-    if (rid == kBadRow) flag_error(P.err);
-    s_rowid[i] = rid;
-  }
-  __syncthreads();
-
-  auto issue = [&](int tile, int stage) {
-    const int li = tile * kTile + warp * 16 + (lane & 15) - tok0;
-    const uint32_t rid = (lane < 16 && li < ntok) ? s_rowid[li] : kBadRow;
-    const uint32_t vm = __ballot_sync(0xffffffffu, rid != kBadRow) & 0xffffu;
-    if (lane == 0) s_vmask[warp][stage] = vm;
-    uint8_t* dst_base = my + stage * kSlab;
-    const int chunk = lane & 15, is_v = lane >> 4;
+  // KV row ids of the selected tokens tok[u] (u < NB) into
+  // s_rowid[i0 + u * kThreads]; entries at or past cn are not touched.
+  // (pages are a power of two in practice: shift and mask instead of a
+  // division there)
+  const bool page_pow2 = (P.page & (P.page - 1)) == 0;
+  const int page_shift = __ffs(P.page) - 1;
+  auto resolve = [&](auto& tok, int i0, int cn) {
+    constexpr int NB = sizeof(tok) / sizeof(tok[0]);
+    int pid[NB], off[NB];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
-      const bool okj = (vm >> j) & 1u;
-      uint8_t* dst = dst_base + is_v * 4096 + j * 256 + ((chunk ^ (j & 7)) << 4);
-      const uint16_t* src = P.kv + static_cast<long long>(okj ? rj : 0u) * 256 + is_v * 128 + chunk * 8;
-      cp_async16(dst, src, okj ? 16u : 0u);
+    for (int u = 0; u < NB; ++u) {
+      const int blk = tok[u] < 0 ? -1 : page_pow2 ? tok[u] >> page_shift : tok[u] / P.page;
+      off[u] = tok[u] - blk * P.page;
+      pid[u] = -1;
+      if (tok[u] >= 0 && blk < P.bt_stride) pid[u] = sbt ? s_bt[blk] : bt_row[blk];
+    }
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const int i = i0 + u * kThreads;
+      if (i >= cn) continue;
+      const uint32_t rid = kv_row_id(P, off[u], pid[u], kvh);
+      bad |= rid == kBadRow;
+      s_rowid[i] = rid;
     }
   };
-
+  // The first kFirst entries per thread of the first chunk.
+  {
+    const int cn = min(kMaxTok, ntok);
 #pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < nt) issue(tb + s, s);
-    cp_async_commit();
+    for (int u = 0; u < kFirst; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      if (i >= cn) tk[u] = -1;
+      else if (P.splits != 1) tk[u] = ptok[i];
+    }
+    resolve(tk, threadIdx.x, cn);
   }
-  for (int it = 0; it < nt; ++it) {
-    cp_async_wait<kStages - 2>();
-    __syncwarp();
-    const int stage = it % kStages;
-    const uint8_t* sK = my + stage * kSlab;
-    const uint8_t* sV = sK + 4096;
 
-    // S^T = K.Q^T over 8 K-steps, split over four accumulators so that the
-    // MMAs form four dependent chains of two instead of one of eight
-    float sa[4][4];
+  // The range runs in chunks of at most kMaxTok tokens whose KV row ids are
+  // resolved into shared memory (in batches of kRidBatch loads per thread)
+  // before the chunk's copies start.
+  for (int c0 = 0; c0 < ntok; c0 += kMaxTok) {
+    const int cn = min(kMaxTok, ntok - c0);
+    const int nt = (cn + kTile - 1) / kTile;
+    if (c0 > 0) __syncthreads();  // every warp has issued the previous chunk's copies
+    const int i_begin = c0 == 0 ? kFirst * kThreads : 0;
+    for (int i0 = i_begin + threadIdx.x; i0 < cn; i0 += kRidBatch * kThreads) {
+      int tok[kRidBatch];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) sa[c][0] = sa[c][1] = sa[c][2] = sa[c][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t a[4];
-      const int rl = lane & 15;
-      const int ch = 2 * kk + (lane >> 4);
-      ldmatrix_x4(a, sK + rl * 256 + ((ch ^ (rl & 7)) << 4));
-      mma_bf16_16816(sa[kk & 3], a, qb[kk][0], qb[kk][1]);
+      for (int u = 0; u < kRidBatch; ++u) {
+        const int i = i0 + u * kThreads;
+        tok[u] = i < cn ? ptok[c0 + i] : -1;
+      }
+      resolve(tok, i0, cn);
     }
-    float s[4];
+    __syncthreads();  // all row ids of the chunk are resolved
+
+    auto issue = [&](int tile, int stage) {
+      const int li = tile * kTile + warp * 16 + (lane & 15);
+      const uint32_t rid = (lane < 16 && li < cn) ? s_rowid[li] : kBadRow;
+      const uint32_t vm = __ballot_sync(0xffffffffu, rid != kBadRow) & 0xffffu;
+      if (lane == 0) s_vmask[warp][stage] = vm;
+      uint8_t* dst_base = smem + (stage * kWarps + warp) * kSlab;
+      const int chunk = lane & 15, is_v = lane >> 4;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[e] = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
-    const uint32_t vm = s_vmask[warp][stage];
-    const bool v0 = (vm >> g) & 1u, v1 = (vm >> (g + 8)) & 1u;
-    const float x0 = v0 ? s[0] * sl2 : -INFINITY;  // token g,   head 2t
-    const float x1 = v0 ? s[1] * sl2 : -INFINITY;  // token g,   head 2t+1
-    const float x2 = v1 ? s[2] * sl2 : -INFINITY;  // token g+8, head 2t
-    const float x3 = v1 ? s[3] * sl2 : -INFINITY;  // token g+8, head 2t+1
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
+        const bool okj = (vm >> j) & 1u;
+        uint8_t* dst = dst_base + is_v * 4096 + j * 256 + ((chunk ^ (j & 7)) << 4);
+        const uint16_t* src = P.kv + static_cast<long long>(okj ? rj : 0u) * 256 + is_v * 128 + chunk * 8;
+        cp_async16(dst, src, okj ? 16u : 0u);
+      }
+    };
+
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    for (int s = 0; s < kStages - 1; ++s) {
+      if (s < nt) issue(s, s);
+      cp_async_commit();
     }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float b0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float p0 = exp2f(x0 - b0), p1 = exp2f(x1 - b1);
-    const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
-    // the running sums and the accumulator need rescaling only where a
-    // running max grew (the factor is exactly 1 elsewhere): skipped when no
-    // lane's max moved
-    if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-      const float al0 = exp2f(m0 - b0), al1 = exp2f(m1 - b1);
-      l0 *= al0;
-      l1 *= al1;
+    for (int it = 0; it < nt; ++it) {
+      cp_async_wait<kStages - 2>();
+      __syncwarp();
+      const int stage = it % kStages;
+      const uint8_t* sK = smem + (stage * kWarps + warp) * kSlab;
+      const uint8_t* sV = sK + 4096;
+      // S^T = K.Q^T over 8 K-steps, split over four accumulators so that the
+      // MMAs form four dependent chains of two instead of one of eight
+      float sa[4][4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sa[c][0] = sa[c][1] = sa[c][2] = sa[c][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a[4];
+        const int rl = lane & 15;
+        const int ch = 2 * kk + (lane >> 4);
+        ldmatrix_x4(a, sK + rl * 256 + ((ch ^ (rl & 7)) << 4));
+        mma_bf16_16816(sa[kk & 3], a, qb[kk][0], qb[kk][1]);
+      }
+      float s[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[e] = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
+      const uint32_t vm = s_vmask[warp][stage];
+      const bool v0 = (vm >> g) & 1u, v1 = (vm >> (g + 8)) & 1u;
+      const float x0 = v0 ? s[0] * sl2 : -INFINITY;  // token g,   head 2t
+      const float x1 = v0 ? s[1] * sl2 : -INFINITY;  // token g,   head 2t+1
+      const float x2 = v1 ? s[2] * sl2 : -INFINITY;  // token g+8, head 2t
+      const float x3 = v1 ? s[3] * sl2 : -INFINITY;  // token g+8, head 2t+1
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float b0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float b1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float p0 = exp2f(x0 - b0), p1 = exp2f(x1 - b1);
+      const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
+      // the running sums and the accumulator need rescaling only where a
+      // running max grew (the factor is exactly 1 elsewhere): skipped when no
+      // lane's max moved
+      if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+        const float al0 = exp2f(m0 - b0), al1 = exp2f(m1 - b1);
+        l0 *= al0;
+        l1 *= al1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= al0;
+          o[mt][1] *= al1;
+          o[mt][2] *= al0;
+          o[mt][3] *= al1;
+        }
+      }
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      m0 = mn0;
+      m1 = mn1;
+      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
+        uint32_t a[4];
+        const int tk = (lane & 7) + ((lane >> 4) << 3);
+        const int ch = 2 * mt + ((lane >> 3) & 1);
+        ldmatrix_x4_trans(a, sV + tk * 256 + ((ch ^ (tk & 7)) << 4));
+        mma_bf16_16816(o[mt], a, pb0, pb1);
       }
+      __syncwarp();
+      const int nxt = it + kStages - 1;
+      if (nxt < nt) issue(nxt, nxt % kStages);
+      cp_async_commit();
     }
-    l0 += p0 + p2;
-    l1 += p1 + p3;
-    m0 = mn0;
-    m1 = mn1;
-    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      uint32_t a[4];
-      const int tk = (lane & 7) + ((lane >> 4) << 3);
-      const int ch = 2 * mt + ((lane >> 3) & 1);
-      ldmatrix_x4_trans(a, sV + tk * 256 + ((ch ^ (tk & 7)) << 4));
-      mma_bf16_16816(o[mt], a, pb0, pb1);
-    }
-    __syncwarp();
-    const int nxt = it + kStages - 1;
-    if (nxt < nt) issue(tb + nxt, nxt % kStages);
-    cp_async_commit();
+    cp_async_wait<0>();
   }
-  cp_async_wait<0>();
+  if (bad) flag_error(P.err);
 
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
@@ -301,8 +371,6 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
   }
   __syncthreads();
 
-  const int h = threadIdx.x >> 4;          // 0..7
-  const int d0 = (threadIdx.x & 15) * 8;   // 8 dims per thread
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * kG + h]);
@@ -316,31 +384,30 @@ __global__ void __launch_bounds__(128) gqa_kernel(const GqaParams P) {
     for (int e = 0; e < 8; ++e) acc[e] += co[(w * kG + h) * 128 + d0 + e] * wt;
   }
   const float inv = L > 0.f ? 1.0f / L : 0.f;
-  const int hq = kvh * kG + h;
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] *= inv;
   if (P.splits == 1) {
-    store_out8(P, (static_cast<long long>(row) * P.hq + hq) * 128 + d0, acc);
+    store_out8(P, obase, acc, gate8);
     return;
   }
-  const long long pbase = (static_cast<long long>(split) * P.rows + row) * P.hq + hq;
-  float4* po = reinterpret_cast<float4*>(P.part_o + pbase * 128 + d0);
+  const long long pb = (static_cast<long long>(split) * P.rows + row) * P.hq + hq;
+  float4* po = reinterpret_cast<float4*>(P.part_o + pb * 128 + d0);
   po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  if ((threadIdx.x & 15) == 0) P.part_lse[pbase] = L > 0.f ? M + __log2f(L) : -INFINITY;
+  if ((threadIdx.x & 15) == 0) P.part_lse[pb] = L > 0.f ? M + __log2f(L) : -INFINITY;
   if (P.counters == nullptr) return;  // a separate merge launch follows
-  // The last CTA of this (row, KV head) merges all splits.
+  // The last split of this (row, KV head) to finish merges them all.
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(P.counters + static_cast<long long>(row) * P.hkv + kvh, 1u);
+    const unsigned prev = atomicAdd(P.counters + blockIdx.x, 1u);
     s_last = prev == static_cast<unsigned>(P.splits - 1);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  merge8(P, row, hq, d0);
-  if (threadIdx.x == 0) P.counters[static_cast<long long>(row) * P.hkv + kvh] = 0u;
+  merge8(P, row, hq, d0, gate8);
+  if (threadIdx.x == 0) P.counters[blockIdx.x] = 0u;  // ready for the next launch
 }
 
 // Log-sum-exp merge of the split partials, then bf16 rounding and the gate.
@@ -348,7 +415,10 @@ __global__ void __launch_bounds__(256) gqa_merge_kernel(const GqaParams P) {
   griddep_launch_dependents();
   griddep_wait();  // all split partials are written
   const int row = blockIdx.x;
-  for (int idx = threadIdx.x; idx < P.hq * 16; idx += blockDim.x) merge8(P, row, idx >> 4, (idx & 15) * 8);
+  for (int idx = threadIdx.x; idx < P.hq * 16; idx += blockDim.x) {
+    const int hq = idx >> 4, d0 = (idx & 15) * 8;
+    merge8(P, row, hq, d0, load_gate8(P, (static_cast<long long>(row) * P.hq + hq) * 128 + d0));
+  }
 }
 
 }  // namespace
@@ -391,8 +461,8 @@ cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
     if (e != cudaSuccess) return e;
     pdl = false;  // a memset node sits between this kernel and its predecessor
   }
-  cudaError_t e = launch_kernel(gqa_kernel, dim3(p.rows * p.hkv, p.splits), dim3(128), kSmem, stream,
-                                pdl, p);
+  cudaError_t e = launch_kernel(gqa_kernel, dim3(p.rows * p.hkv, p.splits), dim3(kThreads), kSmem,
+                                stream, pdl, p);
   if (e != cudaSuccess || p.splits == 1 || p.counters != nullptr) return e;
   return launch_kernel(gqa_merge_kernel, dim3(p.rows), dim3(256), 0, stream, true, p);
 }
