@@ -111,8 +111,12 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   __shared__ uint32_t s_vmask[kWarps][kStages];
   __shared__ int s_last;
   uint32_t* s_rowid = reinterpret_cast<uint32_t*>(smem + kPipe);
-  const int row = blockIdx.x / P.hkv;
-  const int kvh = blockIdx.x % P.hkv;
+  // KV-head-major CTA order: the CTAs resident at one time mostly share a
+  // KV head, so the rows of a request that select the same tokens (prefill
+  // chunks, speculative rows) find them in L2
+  const int kvh = blockIdx.x / P.rows;
+  const int row = blockIdx.x - kvh * P.rows;
+  const int pair = row * P.hkv + kvh;  // merge ticket of this (row, KV head)
   const int split = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -400,14 +404,14 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(P.counters + blockIdx.x, 1u);
+    const unsigned prev = atomicAdd(P.counters + pair, 1u);
     s_last = prev == static_cast<unsigned>(P.splits - 1);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   merge8(P, row, hq, d0, gate8);
-  if (threadIdx.x == 0) P.counters[blockIdx.x] = 0u;  // ready for the next launch
+  if (threadIdx.x == 0) P.counters[pair] = 0u;  // ready for the next launch
 }
 
 // Log-sum-exp merge of the split partials, then bf16 rounding and the gate.
