@@ -56,6 +56,11 @@ GQA_SOURCES = ("learned_sparse_attention_gb300/csrc/sparse_gqa.cu",
                "learned_sparse_attention_gb300/csrc/qsa_device.cuh")
 
 
+def unit_of(spec) -> str:
+    """Rows of a prefill chunk are counted as prefill rows, all others as decode tokens."""
+    return "prefill rows/s" if "prefill" in spec.name else "decode tokens/s"
+
+
 def gqa_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -281,16 +286,16 @@ def run_reference(args):
         t_all += secs
     value = rows_total / t_all
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "decode tokens/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit_of(spec),
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * t_all / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": spec.name, "rows": spec.rows, "reqs": spec.reqs},
-        "cpu_baseline": {"value": value, "unit": "decode tokens/s", "cores": cpu_threads(),
+        "cpu_baseline": {"value": value, "unit": unit_of(spec), "cores": cpu_threads(),
                          "kind": "oracle",
                          "sample": f"whole requests of {spec.name} until ~{args.ref_budget}s "
                                    f"of CPU work per step ({rows_total} rows in total)"},
-        "e2e": {"value": value, "unit": "decode tokens/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit_of(spec), "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -463,12 +468,12 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, rows_done, secs = oracle_sample(spec, wl, budget_s=args.ref_budget)
-        cpu = {"value": rate, "unit": "decode tokens/s", "cores": cpu_threads(), "kind": "oracle",
+        cpu = {"value": rate, "unit": unit_of(spec), "cores": cpu_threads(), "kind": "oracle",
                "sample": f"{rows_done} rows (whole requests) of {spec.name}, {secs:.1f} s"}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "decode tokens/s", "n_gpus": world,
+            "metric": METRIC, "value": value, "unit": unit_of(spec), "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3+bf16" if spec.index_dtype == W.DTYPE_E4M3 else "bf16",
@@ -493,7 +498,7 @@ def run_ours(args):
                               "frac": step_gbs / hbm, "algorithmic_bytes_per_step": step_bytes,
                               "parts": parts},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "decode tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": e2e_value, "unit": unit_of(spec), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches_per_step * args.steps,
             "launch": "CUDA graph of one qsa_layer_step call (value); direct calls (e2e)",
