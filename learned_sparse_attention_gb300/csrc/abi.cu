@@ -368,6 +368,7 @@ qsa_status do_topk(const qsa_cfg* cfg, const float* logits, int64_t ld, int32_t 
   }
   p.tickets = tickets;
   p.tickets_per_row = tickets_per_row;
+  p.sms = sm_count();
   return cuda_status(launch_topk(p, stream, pdl));
 }
 

@@ -74,6 +74,7 @@ struct TopkParams {
   CompressParams ring;
   unsigned* tickets;      // [rows, tickets_per_row] split-merge tickets to zero, or null
   int tickets_per_row;
+  int sms;                // multiprocessors of the device (sizes the per-row clusters)
 };
 size_t topk_smem_bytes(int max_visible, int block_topk);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl);

@@ -7,7 +7,8 @@
 // docstring: request-relative token indices padded with -1, trailing column
 // = valid count.
 //
-// One CTA of 1024 threads per row.  The row's V logits are staged in shared
+// Shared-memory variant (rows longer than the register variant covers): one
+// CTA of 1024 threads per row.  The row's V logits are staged in shared
 // memory as order-preserving 32-bit keys; an 8-bit radix select, starting
 // below the bits that the row's smallest and largest keys share and with
 // warp-aggregated histogram atomics, finds the K_b-th largest key T and how
@@ -15,6 +16,8 @@
 // block-wide scan then writes the selected block ids in ascending order, the
 // lower block winning among equal keys.  Rows with V <= K_b select every
 // visible block without reading logits.
+#include <cooperative_groups.h>
+
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
 #include "qsa_launch.cuh"
@@ -290,21 +293,35 @@ __device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
 }
 
 // KPT: keys per thread the loops are unrolled for (4, 8, 16 or 32), the
-// smallest that covers the launch's max_visible with NT threads (512, or 1024
-// when there are fewer rows than half the SMs).
-template <int KPT, int NT>
+// smallest that covers the launch's max_visible with CL * NT threads.
+// NT: 512, or 1024 when there are fewer rows than half the SMs.
+// CL: CTAs per row, one thread-block cluster (1 or 2).  With CL > 1
+// the row's blocks are split in order over the cluster's CTAs; each radix
+// pass sums the CTAs' shared histograms through distributed shared memory,
+// so every CTA reaches the same digit, and one exchange of per-CTA counts
+// places each CTA's selected blocks in the packed row.
+template <int KPT, int NT, int CL>
 __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const TopkParams P) {
+  namespace cg = cooperative_groups;
   constexpr int NW = NT / 32;
-  __shared__ int hist[kBins];
+  constexpr int GT = CL * NT;  // threads per row
+  __shared__ __align__(16) int hist[kBins];
+  __shared__ __align__(16) int s_red[CL > 1 ? kBins : 4];  // summed bins of this CTA's slice
   __shared__ uint32_t cand[kTail];
   __shared__ int scratch[32];
   __shared__ uint32_t s_min[NW], s_max[NW];
   __shared__ int s_digit, s_k, s_cnt, s_ncand;
+  __shared__ uint32_t s_cmm[2];  // this CTA's (min, max) key, read by the cluster
+  __shared__ int s_ccnt[2];      // this CTA's (greater, equal) counts, read by the cluster
 
   griddep_launch_dependents();
-  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int crank = 0;
+  if constexpr (CL > 1) crank = static_cast<int>(cg::this_cluster().block_rank());
+  const int row = blockIdx.x / CL;
+  const int gtid = crank * NT + tid;  // thread index within the row
   // caller inputs only, before the wait
-  if (P.tickets != nullptr && tid < P.tickets_per_row)
+  if (crank == 0 && P.tickets != nullptr && tid < P.tickets_per_row)
     P.tickets[static_cast<long long>(row) * P.tickets_per_row + tid] = 0u;
   for (int i = tid; i < kBins; i += NT) hist[i] = 0;
   if (tid == 0) s_ncand = 0;
@@ -323,17 +340,18 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
     p = V * r - 1;
   }
   const bool take_all = V <= kb;
-  const int kpt = min(KPT, ((V + NT - 1) / NT + 3) & ~3);
-  const int base = tid * kpt;
+  const int kpt = min(KPT, ((V + GT - 1) / GT + 3) & ~3);
+  const int base = gtid * kpt;
   int32_t* prow = P.packed + static_cast<long long>(row) * (W + 1);
   // Inside the layer step this launch also commits the row's raw key to the
   // compressor-state ring: its loads (caller inputs) are issued now, the
   // store after the wait (all pooling reads of the step are done by then).
   RingCommit rc;
   rc.slot = -1;
-  if (P.do_ring && tid >= 32 && tid < 48) rc = ring_commit_prepare(P.ring, row, tid - 32);
+  const bool ring_lane = P.do_ring && crank == 0 && tid >= 32 && tid < 48;
+  if (ring_lane) rc = ring_commit_prepare(P.ring, row, tid - 32);
   griddep_wait();  // logits (and, transitively, the compress kernel) are done
-  if (P.do_ring && tid >= 32 && tid < 48) ring_commit_store(P.ring, rc, tid - 32);
+  if (ring_lane) ring_commit_store(P.ring, rc, tid - 32);
 
   const int nsel = take_all ? V : kb;
   const int tail0 = V * r;
@@ -383,6 +401,22 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
       kmin = min(kmin, s_min[w]);
       kmax = max(kmax, s_max[w]);
     }
+    if constexpr (CL > 1) {
+      // the row's min and max over the cluster (this sync also orders every
+      // CTA's initialisation before any remote access below)
+      if (tid == 0) {
+        s_cmm[0] = kmin;
+        s_cmm[1] = kmax;
+      }
+      cg::cluster_group cluster = cg::this_cluster();
+      cluster.sync();
+#pragma unroll
+      for (int c = 0; c < CL; ++c) {
+        const uint32_t* o = cluster.map_shared_rank(s_cmm, c);
+        kmin = min(kmin, o[0]);
+        kmax = max(kmax, o[1]);
+      }
+    }
     // Bits above the highest bit where the smallest and largest keys differ
     // are common to every key: the radix passes start below them.
     const uint32_t diff = kmin ^ kmax;
@@ -406,15 +440,45 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
 #pragma unroll
       for (int j = 0; j < KPT; ++j)
         if (key[j] != 0u && (key[j] & pmask) == prefix) atomicAdd(&hist[(key[j] >> shift) & dmask], 1);
-      __syncthreads();
       // bins from the top: thread t holds BPT consecutive bins
       constexpr int BPT = kBins / NT;
       int c[BPT], tot = 0;
+      if constexpr (CL == 1) {
+        __syncthreads();
 #pragma unroll
-      for (int u = 0; u < BPT; ++u) {
-        c[u] = hist[kBins - 1 - BPT * tid - u];
-        hist[kBins - 1 - BPT * tid - u] = 0;  // clear for a further pass
-        tot += c[u];
+        for (int u = 0; u < BPT; ++u) {
+          c[u] = hist[kBins - 1 - BPT * tid - u];
+          hist[kBins - 1 - BPT * tid - u] = 0;  // clear for a further pass
+          tot += c[u];
+        }
+      } else {
+        // The row's histogram is the sum of the cluster's CTA histograms:
+        // CTA q sums bins [q S, (q + 1) S) over the cluster into its s_red
+        // (16-byte remote loads), then every thread reads its four bins
+        // from their owner.  Remote accesses are few and wide: distributed
+        // shared memory serves them per thread, not per warp.
+        static_assert(BPT == 4, "one 16-byte chunk of bins per thread");
+        constexpr int S = kBins / CL;
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();  // every CTA's histogram is complete
+        for (int ch = tid; ch < S / 4; ch += NT) {
+          int4 acc = make_int4(0, 0, 0, 0);
+#pragma unroll
+          for (int q = 0; q < CL; ++q) {
+            const int4 v = *reinterpret_cast<const int4*>(cluster.map_shared_rank(hist, q) + crank * S + 4 * ch);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+          }
+          *reinterpret_cast<int4*>(s_red + crank * S + 4 * ch) = acc;
+        }
+        cluster.sync();  // all slices are summed; no CTA reads a histogram any more
+        const int b0 = kBins - BPT * (tid + 1);  // this thread's lowest bin
+        const int4 v = *reinterpret_cast<const int4*>(cluster.map_shared_rank(s_red, b0 / S) + b0);
+        c[0] = v.w; c[1] = v.z; c[2] = v.y; c[3] = v.x;
+#pragma unroll
+        for (int u = 0; u < BPT; ++u) {
+          hist[kBins - 1 - BPT * tid - u] = 0;
+          tot += c[u];
+        }
       }
       int total;
       int cum = block_sum_excl<NW>(tot, scratch, &total);  // keys in higher bins
@@ -436,12 +500,20 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
       if (hi >= 0 && cnt <= kTail) {
         // The chosen bin holds at most 32 keys: gather them, and one warp
         // sorts them in descending order (bitonic network over the lanes).
+        // (with a cluster, all CTAs append to the first CTA's list)
+        uint32_t* cl_cand = cand;
+        int* cl_ncand = &s_ncand;
+        if constexpr (CL > 1) {
+          cl_cand = cg::this_cluster().map_shared_rank(cand, 0);
+          cl_ncand = cg::this_cluster().map_shared_rank(&s_ncand, 0);
+        }
 #pragma unroll
         for (int j = 0; j < KPT; ++j)
-          if (key[j] != 0u && (key[j] & pmask) == prefix) cand[atomicAdd(&s_ncand, 1)] = key[j];
-        __syncthreads();
+          if (key[j] != 0u && (key[j] & pmask) == prefix) cl_cand[atomicAdd(cl_ncand, 1)] = key[j];
+        if constexpr (CL == 1) __syncthreads();
+        else cg::this_cluster().sync();
         if (warp == 0) {
-          uint32_t v = lane < cnt ? cand[lane] : 0u;
+          uint32_t v = lane < cnt ? cl_cand[lane] : 0u;
 #pragma unroll
           for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
@@ -476,7 +548,21 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
     // the first keq equal keys in block order
     int tot;
     const int both = block_sum_excl<NW>((__popc(gt_mask) << 16) | __popc(eq_mask), scratch, &tot);
-    const int gt_before = both >> 16, eq_before = both & 0xFFFF;
+    int gt_before = both >> 16, eq_before = both & 0xFFFF;
+    if constexpr (CL > 1) {
+      // counts of the CTAs holding lower blocks
+      if (tid == 0) {
+        s_ccnt[0] = tot >> 16;
+        s_ccnt[1] = tot & 0xFFFF;
+      }
+      cg::cluster_group cluster = cg::this_cluster();
+      cluster.sync();
+      for (int c = 0; c < crank; ++c) {
+        const int* o = cluster.map_shared_rank(s_ccnt, c);
+        gt_before += o[0];
+        eq_before += o[1];
+      }
+    }
     int take = keq - eq_before;
     take = take < 0 ? 0 : take;
     uint32_t eq_take = eq_mask;
@@ -492,17 +578,19 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
       m &= m - 1u;
     }
     // the tail tokens of the open group, then -1 padding
-    for (int idx = nsel * r + tid; idx < W; idx += NT)
+    for (int idx = nsel * r + gtid; idx < W; idx += GT)
       prow[idx] = idx < count ? tail0 + (idx - nsel * r) : -1;
+    // no CTA leaves while another may still read its shared memory
+    if constexpr (CL > 1) cg::this_cluster().sync();
   } else {
-    for (int idx = tid; idx < W; idx += NT) {
+    for (int idx = gtid; idx < W; idx += GT) {
       int v = -1;
       if (idx < nsel * r) v = idx;  // block idx / r, token idx % r
       else if (idx < count) v = tail0 + (idx - nsel * r);
       prow[idx] = v;
     }
   }
-  if (tid == 0) prow[W] = count;
+  if (gtid == 0) prow[W] = count;
 }
 
 }  // namespace
@@ -514,17 +602,32 @@ size_t topk_smem_bytes(int max_visible, int block_topk) {
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
   if (p.max_visible <= kRegKeys * kRegThreads && p.token_topk / p.ratio <= kRegKeys * kRegThreads / 4) {
-    // few rows: twice the threads per row, half the keys per thread
+    const dim3 b(kRegThreads);
+    // Many rows with long key lists: a cluster of two 512-thread CTAs per
+    // row (half the keys per thread) while the rows' CTAs still fit one wave
+    // at two per SM.  Measured: fewer rows gain nothing from clusters over
+    // one 1024-thread CTA per row (below), and larger clusters cost more in
+    // cluster barriers than they save.
+    const long long slots = 2LL * (p.sms > 0 ? p.sms : 1);
+    if (p.rows >= 76 && 2LL * p.rows <= slots && p.max_visible > 4 * 1024) {
+      const int kpt = (p.max_visible + 2 * kRegThreads - 1) / (2 * kRegThreads);
+      const dim3 g(p.rows * 2);
+      if (kpt <= 4) return launch_kernel_cluster(topk_reg_kernel<4, kRegThreads, 2>, g, b, 0, stream, pdl, 2, p);
+      if (kpt <= 8) return launch_kernel_cluster(topk_reg_kernel<8, kRegThreads, 2>, g, b, 0, stream, pdl, 2, p);
+      return launch_kernel_cluster(topk_reg_kernel<16, kRegThreads, 2>, g, b, 0, stream, pdl, 2, p);
+    }
+    // few rows, short keys: twice the threads per row, half the keys per thread
     if (p.rows < 76 && p.max_visible > 4 * 1024) {
       const int kpt = (p.max_visible + 1023) / 1024;
-      if (kpt <= 8) return launch_kernel(topk_reg_kernel<8, 1024>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
-      return launch_kernel(topk_reg_kernel<16, 1024>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
+      if (kpt <= 8) return launch_kernel(topk_reg_kernel<8, 1024, 1>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
+      return launch_kernel(topk_reg_kernel<16, 1024, 1>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
     }
     const int kpt = (p.max_visible + kRegThreads - 1) / kRegThreads;
-    if (kpt <= 4) return launch_kernel(topk_reg_kernel<4, kRegThreads>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
-    if (kpt <= 8) return launch_kernel(topk_reg_kernel<8, kRegThreads>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
-    if (kpt <= 16) return launch_kernel(topk_reg_kernel<16, kRegThreads>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
-    return launch_kernel(topk_reg_kernel<32, kRegThreads>, dim3(p.rows), dim3(kRegThreads), 0, stream, pdl, p);
+    const dim3 g(p.rows);
+    if (kpt <= 4) return launch_kernel(topk_reg_kernel<4, kRegThreads, 1>, g, b, 0, stream, pdl, p);
+    if (kpt <= 8) return launch_kernel(topk_reg_kernel<8, kRegThreads, 1>, g, b, 0, stream, pdl, p);
+    if (kpt <= 16) return launch_kernel(topk_reg_kernel<16, kRegThreads, 1>, g, b, 0, stream, pdl, p);
+    return launch_kernel(topk_reg_kernel<32, kRegThreads, 1>, g, b, 0, stream, pdl, p);
   }
   const size_t smem = topk_smem_bytes(p.max_visible, p.token_topk / p.ratio);
   cudaError_t e =

@@ -149,15 +149,20 @@ def test_index_logits_matches_oracle(name):
     (4, 2048, [8191, 20000, 32767, 2046, 2047, 8000]),
     (8, 4096, [131071, 65535, 32767, 1000]),
     (2, 256, [1, 5, 511, 512, 999]),
+    # enough rows for the two-CTA cluster per row (8 and 16 keys per thread)
+    (4, 2048, [16384 + 207 * i for i in range(80)]),
+    (8, 4096, [131071 - 997 * i for i in range(100)]),
 ])
-@pytest.mark.parametrize("ties", [False, True])
+@pytest.mark.parametrize("ties", [False, True, "all_equal"])
 def test_topk_matches_oracle(ratio, topk, positions, ties):
     cfg_o = O.QsaConfig(n_heads=8, compress_ratio=ratio, token_topk=topk)
     cfg = Q.make_cfg(8, ratio, topk, BF, 16, 10)
     logical = np.array(positions, dtype=np.int32)
     mv = int(max((p + 1) // ratio for p in positions))
-    rng = np.random.default_rng(ratio * 1000 + topk + ties)
-    if ties:  # few distinct values: many exact ties at the selection boundary
+    rng = np.random.default_rng(ratio * 1000 + topk + (ties is True))
+    if ties == "all_equal":  # every key ties: the lowest blocks are taken
+        vals = np.full((len(positions), mv), 0.25, dtype=np.float32)
+    elif ties:  # few distinct values: many exact ties at the selection boundary
         vals = rng.integers(0, 7, size=(len(positions), mv)).astype(np.float32) / 8
     else:
         vals = rng.standard_normal((len(positions), mv)).astype(np.float32)
