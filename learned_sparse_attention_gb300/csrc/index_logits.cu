@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   unsigned long long* err = P.err;
-  griddep_wait();  // the query tile and this step's compressed keys are written
+  // The TMA producer waits later, after issuing the tiles that hold no key
+  // this step's compress kernel can write; every other warp waits here.
+  if (!(TMA && warp == 1)) griddep_wait();  // the query tile and this step's compressed keys are written
 
   if (warp == 0) {
     // ------------------------------------------------------ B tile + MMA issuer
@@ -236,11 +238,23 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
     // every lane issues its box.  Pages past the group's keys are skipped
     // (those rows are never stored); an out-of-range page id is read as
     // zeros, written before the barrier is armed.
+    //
+    // The compress kernel of this step writes only the compressed keys of
+    // groups that hold one of this step's tokens: for a request whose first
+    // new token is at position f (its rows are consecutive positions), keys
+    // below floor(f / ratio) are caller inputs.  The ring's first tiles
+    // made only of such keys are issued before the dependency wait, so
+    // their gather overlaps the compress kernel.
     if (warp == 1) {
       const int nbox = C::ATOMS * ppt;  // <= 32 for cpage >= 8
       const uint32_t box_bytes = static_cast<uint32_t>(cpage) * 128u;
       const int elems_per_atom = 128 / (IDT == 1 ? 1 : 2);
+      const int f = min(P.logical[P.qsl[req]], P.logical[row0]);
+      const int c_safe = f < 0 ? 0 : f / P.ratio;
+      const int n_early = max(0, min(min(ntiles, C::STAGES), c_safe / 128 - t_begin));
+      if (n_early == 0) griddep_wait();
       for (int i = 0; i < ntiles; ++i) {
+        if (i == n_early && n_early > 0) griddep_wait();
         const int s = i % C::STAGES;
         const uint32_t ph = (i / C::STAGES) & 1;
         bool ok = true;

@@ -3,13 +3,36 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 namespace qsa {
+
+// Every kernel asks for the largest shared-memory carveout, once per device:
+// the kernels of a layer step, chained with programmatic dependent launch,
+// then run under one SM configuration, so the CTAs of a kernel that starts
+// early never wait for its predecessor's CTAs to leave an SM before the SM
+// can be reconfigured for their shared memory.
+inline cudaError_t prefer_max_smem(const void* fn) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({dev, fn})) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess) done.insert({dev, fn});
+  return e;
+}
 
 // pdl: the kernel may start before the previous kernel on the stream
 // finishes; it calls griddep_wait() before reading that kernel's results.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                           cudaStream_t stream, bool pdl, Args&&... args) {
+  const cudaError_t ce = prefer_max_smem(reinterpret_cast<const void*>(kernel));
+  if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -27,6 +50,8 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                   cudaStream_t stream, bool pdl, int cluster_x, Args&&... args) {
+  const cudaError_t ce = prefer_max_smem(reinterpret_cast<const void*>(kernel));
+  if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
