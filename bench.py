@@ -51,7 +51,7 @@ def flush_l2(flush, drain, i):
 # DRAM bytes per launch of the sparse GQA kernel on the decode batch, from one
 # ncu capture (the decode-batch kernel-sections summary), keyed by a hash of
 # the kernel sources it was taken on; any other source reports null.
-GQA_TRAFFIC = {"a32145a37ab81122": 270416896 + 3225856}
+GQA_TRAFFIC = {"74bde55c61c42a04": 270416896 + 3225856}
 GQA_SOURCES = ("learned_sparse_attention_gb300/csrc/sparse_gqa.cu",
                "learned_sparse_attention_gb300/csrc/qsa_device.cuh")
 
@@ -62,11 +62,17 @@ def unit_of(spec) -> str:
 
 
 def gqa_source_hash() -> str:
+    """Hash of the GQA kernel sources with comments and blank lines removed
+    (a comment edit does not change the kernel the counters were taken on)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in GQA_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            for line in fh:
+                code = re.sub(r"//.*", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -21,9 +21,13 @@
 // P^T comes from the S^T accumulator with one movmatrix transpose per 8x8
 // block; each lane keeps the online-softmax state of its two heads, the same
 // heads its O^T fragments hold.  The four warps are merged in shared memory.
-// A prologue resolves the CTA's whole token range (packed index -> block
-// table -> KV row id) into shared memory in parallel, so the copy issue of a
-// slab never waits on a dependent global load.  With split-KV, the last CTA
+// A prologue resolves the CTA's token range (packed index -> block table ->
+// KV row id, in chunks of up to 2560 tokens) into shared memory in parallel,
+// so the copy issue of a slab never waits on a dependent global load; the
+// inputs that do not depend on the top-k kernel (q, gate, the request's
+// block-table row) are loaded before the dependency wait, and the first
+// chunk's packed entries together with the count right after it.  CTAs run
+// in KV-head-major order.  With split-KV, the last CTA
 // of a (row, KV head) to finish merges the fp32 partials (an atomic ticket
 // per (row, KV head)), so no second launch is needed when a ticket array is
 // given.
@@ -43,8 +47,8 @@ constexpr int kTile = 64;      // tokens per CTA tile (16 per warp)
 constexpr int kStages = 3;
 constexpr int kSlab = 16 * 512;  // bytes per warp stage: 16 tokens x (K|V)
 constexpr int kPipe = kWarps * kStages * kSlab;
-constexpr int kMaxTiles = 40;                // tiles of one CTA
-constexpr int kMaxTok = kMaxTiles * kTile;   // token row ids staged per CTA
+constexpr int kMaxTiles = 40;                // tiles of one row-id chunk
+constexpr int kMaxTok = kMaxTiles * kTile;   // token row ids staged at a time
 constexpr int kSmem = kPipe + kMaxTok * 4;
 constexpr uint32_t kBadRow = 0xFFFFFFFFu;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -427,8 +431,9 @@ __global__ void __launch_bounds__(256) gqa_merge_kernel(const GqaParams P) {
 
 }  // namespace
 
-// Split-KV count: at least one CTA per SM, and no CTA with more than
-// kMaxTiles 64-token tiles (its row ids are staged in shared memory).
+// Split-KV count: about two CTAs per SM of a GB300 (152 SMs), and no CTA with
+// more than kMaxTiles 64-token tiles (one chunk of staged row ids, so that
+// the request's block-table row is read from shared memory).
 int gqa_num_splits(int rows, int hkv, int packed_width) {
   const long long base = static_cast<long long>(rows) * hkv;
   if (base <= 0) return 1;
