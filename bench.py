@@ -56,6 +56,33 @@ GQA_SOURCES = ("learned_sparse_attention_gb300/csrc/sparse_gqa.cu",
                "learned_sparse_attention_gb300/csrc/qsa_device.cuh")
 
 
+# The inputs a layer step takes from its caller each step (the rest is state
+# or configuration that stays on the device).
+STEP_INPUTS = ("projected_q", "raw_keys", "positions", "q", "gate", "token_to_req",
+               "query_start_loc", "logical_positions", "compressed_slots")
+
+
+def pack_step_inputs(t: dict, keys, device, pin: bool):
+    """One host buffer (pinned if `pin`) and one device buffer holding the
+    tensors t[k] for k in keys in 256-byte aligned slots.  Returns (host
+    buffer, device buffer, a copy of t whose entries for keys are slices of
+    the device buffer); copying the host buffer into the device buffer sets
+    all of them."""
+    offs, total = [], 0
+    for k in keys:
+        offs.append(total)
+        total += (t[k].numel() * t[k].element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=pin)
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=device)
+    views = dict(t)
+    for k, off in zip(keys, offs):
+        src = t[k].contiguous()
+        nb = src.numel() * src.element_size()
+        host_buf[off:off + nb].copy_(src.reshape(-1).view(torch.uint8).cpu())
+        views[k] = dev_buf[off:off + nb].view(src.dtype).view(src.shape)
+    return host_buf, dev_buf, views
+
+
 def unit_of(spec) -> str:
     """Rows of a prefill chunk are counted as prefill rows, all others as decode tokens."""
     return "prefill rows/s" if "prefill" in spec.name else "decode tokens/s"
@@ -447,23 +474,10 @@ def run_ours(args):
     # The step's inputs sit in one pinned host buffer (256-byte aligned
     # slots) and travel in one copy to one device buffer whose slices are the
     # step's input tensors.
-    inputs = ["projected_q", "raw_keys", "positions", "q", "gate", "token_to_req",
-              "query_start_loc", "logical_positions", "compressed_slots"]
-    offs, total = [], 0
-    for k in inputs:
-        offs.append(total)
-        total += (wl.t[k].numel() * wl.t[k].element_size() + 255) // 256 * 256
-    host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-    dev_buf = torch.empty(total, dtype=torch.uint8, device=device)
-    t_e2e = dict(wl.t)
-    for k, off in zip(inputs, offs):
-        src = wl.t[k].contiguous()
-        nb = src.numel() * src.element_size()
-        host_buf[off:off + nb].copy_(src.reshape(-1).view(torch.uint8).cpu())
-        t_e2e[k] = dev_buf[off:off + nb].view(src.dtype).view(src.shape)
+    host_buf, dev_buf, t_e2e = pack_step_inputs(wl.t, STEP_INPUTS, device, pin=True)
     sargs_e2e = Q.step_args(t_e2e, packed, out, mv)
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(wl.t[k].numel() * wl.t[k].element_size() for k in inputs)
+    h2d = sum(wl.t[k].numel() * wl.t[k].element_size() for k in STEP_INPUTS)
     d2h = out_host.numel() * out_host.element_size()
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
