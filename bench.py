@@ -7,7 +7,13 @@ the decode tokens/s metric is quoted on.  One step = one call of
 qsa_layer_step (all four stages) over that batch.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload NAME] [--no-cpu-baseline] [--no-extra]
+
+The default run also reports, in the same JSON line, the other workloads of
+the metric: the chunked prefill (rows/s, the index-logits kernel against a
+dense-fp8 peak measured in the same run, sparse GQA against its bf16 FLOPs),
+the long-context decode and the MTP verify draft (step 0 plus three skip_topk
+steps captured as one CUDA graph of qsa_mtp_steps).
 
 N > 1 runs under torchrun as independent replicas (one per GPU, no
 collective on the data path: requests are independent), value = total rows
@@ -81,6 +87,66 @@ def pack_step_inputs(t: dict, keys, device, pin: bool):
         host_buf[off:off + nb].copy_(src.reshape(-1).view(torch.uint8).cpu())
         views[k] = dev_buf[off:off + nb].view(src.dtype).view(src.shape)
     return host_buf, dev_buf, views
+
+
+def config_of(spec, world: int) -> dict:
+    """The workload description printed by both arms."""
+    return {"workload": spec.name, "rows": spec.rows, "reqs": spec.reqs,
+            "contexts": f"{min(spec.contexts)}..{max(spec.contexts)}",
+            "indexer": f"{spec.n_heads}x128 {'e4m3' if spec.index_dtype else 'bf16'}"
+                       f" r={spec.compress_ratio} topk={spec.token_topk}",
+            "gqa": f"{spec.hq}q/{spec.hkv}kv x128 bf16 page {spec.page}",
+            "parallelism": f"replicas x{world}",
+            "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, then a "
+                  f"{DRAIN_BYTES >> 20} MiB read to evict the written lines)"}
+
+
+def measure_fp8_peak(device, n=8192, reps=10):
+    """Dense e4m3 x e4m3 -> bf16 GEMM throughput of the library GEMM
+    (torch._scaled_mm, n^3, best of `reps`, CUDA events): the fp8 tensor
+    peak the prefill index-logits kernel is quoted against."""
+    try:
+        a = torch.randn((n, n), device=device).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device=device).to(torch.float8_e4m3fn).t()  # column-major
+        one = torch.ones((), device=device, dtype=torch.float32)
+        fn = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        torch.cuda.empty_cache()
+        return {"fp8_tflops": 2.0 * n ** 3 / (best / 1000.0) / 1e12, "ms": best,
+                "how": f"torch._scaled_mm e4m3 {n}^3 -> bf16, best of {reps}, CUDA events"}
+    except Exception as e:  # no fp8 GEMM in this torch build
+        return {"fp8_tflops": None, "error": str(e)[:200]}
+
+
+class CpuClock:
+    """Wall and process CPU time around a region: cores = CPU s / wall s is
+    the number of cores the region actually kept busy (BLAS threads included)."""
+
+    def __init__(self):
+        self.wall = self.cpu = 0.0
+
+    def __enter__(self):
+        self.w0, self.c0 = time.perf_counter(), time.process_time()
+        return self
+
+    def __exit__(self, *exc):
+        self.wall += time.perf_counter() - self.w0
+        self.cpu += time.process_time() - self.c0
+
+    @property
+    def cores(self) -> float:
+        return round(self.cpu / self.wall, 2) if self.wall > 0 else 0.0
 
 
 def unit_of(spec) -> str:
@@ -263,7 +329,8 @@ def oracle_sample(spec, wl, budget_s=15.0, max_rows=None):
 
     st = OracleState(wl, with_kv=False)
     qsl = st.query_start_loc
-    done_rows, spent = 0, 0.0
+    done_rows = 0
+    clock = CpuClock()
     for req in range(spec.reqs):
         a, b = int(qsl[req]), int(qsl[req + 1])
         if b <= a:
@@ -284,20 +351,50 @@ def oracle_sample(spec, wl, budget_s=15.0, max_rows=None):
             compressed_slots=st.compressed_slots[a:b],
             cblock_table=st.cblock_table[req:req + 1], q=st.q[a:b], kv=kv,
             block_table=np.arange(nblk)[None, :], page=spec.page, gate=st.gate[a:b])
-        t0 = time.perf_counter()
-        O.layer_step(st.cfg, **sub)
-        spent += time.perf_counter() - t0
+        with clock:
+            O.layer_step(st.cfg, **sub)
         done_rows += len(rows)
-        if spent >= budget_s or (max_rows and done_rows >= max_rows):
+        if clock.wall >= budget_s or (max_rows and done_rows >= max_rows):
             break
-    return done_rows / spent, done_rows, spent
+    return done_rows / clock.wall, done_rows, clock.wall, clock.cores
 
 
-def cpu_threads():
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
-        if os.environ.get(k):
-            return int(os.environ[k])
-    return os.cpu_count()
+def oracle_prefill_sample(spec, wl, nsample=192, seed=0):
+    """The oracle on the chunked prefill: stage 1's pooling of every group the
+    chunk completes (timed in full), then query prep, selection and sparse
+    GQA of `nsample` seeded rows, extrapolated linearly to all rows.
+    Returns (rows/s, seconds of the extrapolated step, cores, sample text)."""
+    from oracle import qsa_oracle as O
+    from tests.oracle_io import OracleState, f64
+
+    st = OracleState(wl, with_kv=False)
+    L = int(st.logical_positions[-1]) + 1
+    nblk = -(-L // spec.page)
+    kv = f64(wl["kv"][torch.as_tensor(st.block_table[0, :nblk], device=wl["kv"].device)])
+    rows = np.sort(np.random.default_rng(seed).choice(spec.rows, size=nsample, replace=False))
+    c1, c2 = CpuClock(), CpuClock()
+    with c1:
+        O.compress_stage(st.cfg, projected_q=None, raw_keys=st.raw_keys, positions=st.positions,
+                         cos_sin=st.cos_sin, q_norm_w=st.q_norm_w, k_norm_w=st.k_norm_w,
+                         ring=st.ring, ring_pos=st.ring_pos,
+                         ring_block_table=st.ring_block_table, token_to_req=st.token_to_req,
+                         query_start_loc=st.query_start_loc,
+                         logical_positions=st.logical_positions, ccache=st.ccache,
+                         compressed_slots=st.compressed_slots)
+    with c2:
+        for row in rows:
+            q_idx = O.prep_query(st.cfg, st.projected_q[row], st.positions[row], st.cos_sin,
+                                 st.q_norm_w)
+            _, _, packed = O.select_row(st.cfg, q_idx, st.ccache, st.cblock_table[0],
+                                        int(st.logical_positions[row]))
+            n = int(packed[-1])
+            O.sparse_gqa_row(st.q[row], kv, np.arange(nblk), packed[:n], spec.page, st.gate[row])
+    total = c1.wall + c2.wall * spec.rows / nsample
+    cores = round((c1.cpu + c2.cpu) / (c1.wall + c2.wall), 2)
+    text = (f"stage-1 pooling of all {int((st.compressed_slots >= 0).sum())} groups "
+            f"({c1.wall:.1f} s) + query prep, selection and sparse GQA of {nsample} seeded rows "
+            f"({c2.wall:.1f} s) extrapolated x{spec.rows / nsample:.1f} to {spec.rows} rows")
+    return spec.rows / total, total, cores, text
 
 
 # --------------------------------------------------------------------------- arms
@@ -310,21 +407,20 @@ def run_reference(args):
     wl = W.make_workload(spec, device=device)
     for _ in range(args.warmup):
         oracle_sample(spec, wl, budget_s=0.0, max_rows=1)
-    times, rows_total = [], 0
-    t_all = 0.0
+    rows_total, t_all, cores = 0, 0.0, []
     for _ in range(args.steps):
-        rate, rows, secs = oracle_sample(spec, wl, budget_s=args.ref_budget)
-        times.append(secs)
+        rate, rows, secs, c = oracle_sample(spec, wl, budget_s=args.ref_budget)
         rows_total += rows
         t_all += secs
+        cores.append(c)
     value = rows_total / t_all
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit_of(spec),
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * t_all / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": spec.name, "rows": spec.rows, "reqs": spec.reqs},
-        "cpu_baseline": {"value": value, "unit": unit_of(spec), "cores": cpu_threads(),
+        "config": config_of(spec, 1),
+        "cpu_baseline": {"value": value, "unit": unit_of(spec), "cores": max(cores),
                          "kind": "oracle",
                          "sample": f"whole requests of {spec.name} until ~{args.ref_budget}s "
                                    f"of CPU work per step ({rows_total} rows in total)"},
@@ -335,31 +431,133 @@ def run_reference(args):
     return 0
 
 
-def prefill_report(device, steps, flush, drain):
+def capture(fn, device):
+    """One CUDA graph of fn (a sequence of C-ABI calls without host sync)."""
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    torch.cuda.synchronize()
+    return graph
+
+
+def timed(fn, steps, flush, drain):
+    """Per-call CUDA-event times (ms) on the current stream, the L2 flushed
+    and drained before every call, outside the events."""
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(flush, drain, i)
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def gqa_kernel_ms(wl, gcfg, packed, out, ws, steps, flush, drain):
+    """The sparse GQA stage alone (the dominant kernel of a decode step)."""
+    ts = timed(lambda: Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], packed,
+                                    wl["token_to_req"], wl["gate"], out, ws), steps, flush, drain)
+    return statistics.mean(ts)
+
+
+def hbm_line(achieved_bytes, ms, hbm):
+    gbs = achieved_bytes / (ms / 1000.0) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+            "algorithmic_bytes": achieved_bytes, "ms": ms}
+
+
+def decode_report(name, device, steps, warmup, flush, drain, hbm):
+    """A decode workload other than the headline one: graph-replayed layer
+    step (tokens/s, step against HBM) and its sparse GQA kernel alone."""
+    spec = W.named_spec(name)
+    wl, cfg, gcfg, mv, packed, out, ws = build(spec, device)
+    sargs = Q.step_args(wl.t, packed, out, mv)
+    for _ in range(warmup):
+        Q.layer_step(cfg, gcfg, sargs, ws)
+    graph = capture(lambda: Q.layer_step(cfg, gcfg, sargs, ws), device)
+    for _ in range(warmup):
+        graph.replay()
+    ms = statistics.mean(timed(graph.replay, steps, flush, drain))
+    g_ms = gqa_kernel_ms(wl, gcfg, packed, out, ws, steps, flush, drain)
+    if Q.check_errors() != 0:
+        raise RuntimeError(f"device error word set during {name}")
+    step_bytes, gqa_bytes, parts = algorithmic_bytes(spec, wl, packed)
+    res = {"workload": name, "rows": spec.rows, "ms_per_step": ms, "steps": steps,
+           "value": spec.rows / (ms / 1000.0), "unit": "decode tokens/s",
+           "step_roofline": hbm_line(step_bytes, ms, hbm), "parts": parts,
+           "gqa_roofline": hbm_line(gqa_bytes, g_ms, hbm),
+           "launches_per_step": Q.step_launches(cfg, gcfg, spec.rows, spec.reqs)}
+    del wl, packed, out, ws, graph
+    torch.cuda.empty_cache()
+    return res
+
+
+def mtp_report(device, steps, warmup, flush, drain, hbm):
+    """The MTP verify draft with MRoPE: step 0 selects, steps 1-3 reuse its
+    packed buffer (skip_topk) with fresh per-step inputs.  The four steps are
+    one qsa_mtp_steps call captured as one CUDA graph and replayed after an
+    L2 flush; tokens/s counts every row once per step.  Step 0 and a skip
+    step are also timed alone for the breakdown."""
+    spec = W.named_spec("mtp_mrope")
+    k = spec.mtp_steps
+    wl, cfg, gcfg, mv, packed, out, ws = build(spec, device)
+    per_step, outs = [], []
+    for s in range(k):
+        fresh = W.make_workload(spec, device=device, step=s, with_caches=False)
+        t = dict(wl.t)
+        for n in ("projected_q", "raw_keys", "positions", "q", "gate"):
+            t[n] = fresh[n]
+        outs.append(torch.empty_like(wl["q"]))
+        per_step.append(Q.step_args(t, packed, outs[-1], mv))
+    draft = lambda: Q.mtp_steps(cfg, gcfg, per_step, ws)
+    for _ in range(warmup):
+        draft()
+    g_all = capture(draft, device)
+    g0 = capture(lambda: Q.layer_step(cfg, gcfg, per_step[0], ws), device)
+    g1 = capture(lambda: Q.layer_step(cfg, gcfg, per_step[1], ws, skip_topk=True), device)
+    for _ in range(warmup):
+        g_all.replay()
+    cycle_ms = statistics.mean(timed(g_all.replay, steps, flush, drain))
+    s0_ms = statistics.mean(timed(g0.replay, steps, flush, drain))
+    s1_ms = statistics.mean(timed(g1.replay, steps, flush, drain))
+    if Q.check_errors() != 0:
+        raise RuntimeError("device error word set during the MTP draft")
+    step_bytes, gqa_bytes, parts = algorithmic_bytes(spec, wl, packed)
+    res = {"workload": spec.name, "rows": spec.rows, "draft_steps": k, "steps": steps,
+           "draft_ms": cycle_ms, "value": k * spec.rows / (cycle_ms / 1000.0),
+           "unit": "decode tokens/s", "step0_ms": s0_ms, "skip_step_ms": s1_ms,
+           "step0_roofline": hbm_line(step_bytes, s0_ms, hbm), "parts_step0": parts,
+           "launch": "one CUDA graph of qsa_mtp_steps (4 layer steps)",
+           "launches_per_draft": Q.step_launches(cfg, gcfg, spec.rows, spec.reqs)
+           + (k - 1) * Q.step_launches(cfg, gcfg, spec.rows, spec.reqs, skip_topk=True)}
+    del wl, packed, out, ws, outs, per_step, g_all, g0, g1
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_report(device, steps, flush, drain, fp8, bf16, cpu_baseline):
     """The chunked-prefill workload (one request, 16384 new rows after a
-    32768-token prefix): layer-step rows/s, and the index-logits kernel alone
-    against the fp8 tensor peak (FLOPs = visible keys x heads x 128 x 2)."""
+    32768-token prefix): layer-step rows/s; the index-logits kernel alone
+    against the measured dense-fp8 peak (FLOPs = visible keys x heads x 128
+    x 2); the sparse GQA kernel alone against the bf16 peak (FLOPs = 4 x 128
+    x Hq x selected tokens)."""
     spec = W.named_spec("chunked_prefill")
     wl, cfg, gcfg, mv, packed, out, ws = build(spec, device)
     sargs = Q.step_args(wl.t, packed, out, mv)
-    stream = torch.cuda.current_stream()
     for _ in range(2):
         Q.layer_step(cfg, gcfg, sargs, ws)
     torch.cuda.synchronize()
-
-    def timed(fn):
-        ts = []
-        for i in range(steps):
-            flush_l2(flush, drain, i)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
-
-    step_ms = timed(lambda: Q.layer_step(cfg, gcfg, sargs, ws))
+    step_ms = statistics.median(timed(lambda: Q.layer_step(cfg, gcfg, sargs, ws), steps,
+                                      flush, drain))
     t = wl.t
     q_idx = torch.empty((spec.rows, spec.n_heads, 128),
                         dtype=torch.uint8 if spec.index_dtype == W.DTYPE_E4M3 else torch.bfloat16,
@@ -370,21 +568,35 @@ def prefill_report(device, steps, flush, drain):
                t["compressed_slots"])
     logits = torch.empty((spec.rows, (mv + 3) // 4 * 4), dtype=torch.float32, device=device)
     lws = torch.empty(256, dtype=torch.uint8, device=device)
-    logits_ms = timed(lambda: Q.index_logits(cfg, q_idx, t["ccache"], t["cblock_table"],
-                                             t["token_to_req"], t["query_start_loc"],
-                                             t["logical_positions"], logits, mv, lws))
+    logits_ms = statistics.median(timed(
+        lambda: Q.index_logits(cfg, q_idx, t["ccache"], t["cblock_table"], t["token_to_req"],
+                               t["query_start_loc"], t["logical_positions"], logits, mv, lws),
+        steps, flush, drain))
+    gqa_ms = statistics.median(timed(
+        lambda: Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], packed,
+                             wl["token_to_req"], wl["gate"], out, ws), steps, flush, drain))
     if Q.check_errors() != 0:
         raise RuntimeError("device error word set during the prefill measurement")
     vis = ((t["logical_positions"].long() + 1) // spec.compress_ratio).clamp(min=0)
     flops = float(vis.sum()) * spec.n_heads * 128 * 2
-    peaks, peak_kind = load_peaks()
-    fp8 = 2.0 * float(peaks["bf16_tflops"])
     tf = flops / (logits_ms / 1000.0) / 1e12
+    n_sel = float(packed[:, -1].long().sum())
+    gflops = 4.0 * 128 * spec.hq * n_sel
+    gtf = gflops / (gqa_ms / 1000.0) / 1e12
     res = {"workload": spec.name, "rows": spec.rows, "steps": steps,
            "ms_per_step": step_ms, "value": spec.rows / (step_ms / 1000.0), "unit": "prefill rows/s",
-           "index_logits": {"bound": "tensor", "achieved": tf, "peak": fp8, "unit": "TFLOP/s",
-                            "frac": tf / fp8, "kernel_ms": logits_ms, "flops_per_launch": flops,
-                            "peak_source": f"2 x {peak_kind} bf16_tflops (nominal fp8/bf16 ratio)"}}
+           "index_logits": {"bound": "tensor", "achieved": tf, "peak": fp8["fp8_tflops"],
+                            "unit": "TFLOP/s",
+                            "frac": tf / fp8["fp8_tflops"] if fp8.get("fp8_tflops") else None,
+                            "kernel_ms": logits_ms, "flops_per_launch": flops,
+                            "peak_source": "dense fp8 measured in this run: " + fp8.get("how", "")},
+           "sparse_gqa": {"bound": "tensor", "achieved": gtf, "peak": bf16, "unit": "TFLOP/s",
+                          "frac": gtf / bf16, "kernel_ms": gqa_ms, "flops_per_launch": gflops,
+                          "peak_source": "MEASURED_PEAKS bf16_tflops (burst)"}}
+    if cpu_baseline:
+        rate, secs, cores, text = oracle_prefill_sample(spec, wl)
+        res["cpu_baseline"] = {"value": rate, "unit": "prefill rows/s", "cores": cores,
+                               "kind": "oracle", "sample": text}
     del wl, packed, out, ws, logits, q_idx
     torch.cuda.empty_cache()
     return res
@@ -413,57 +625,25 @@ def run_ours(args):
         raise RuntimeError("device error word set during warm-up")
     # The timed step replays one CUDA-graph capture of the same C-ABI call
     # (the call makes no host synchronisation, so it captures as is).
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream(device=device)
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        step_direct()
-    stream.wait_stream(side)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(graph):
-        step_direct()
-    torch.cuda.synchronize()
-
-    def step():
-        graph.replay()
-
+    graph = capture(step_direct, device)
     for _ in range(args.warmup):
-        step()
+        graph.replay()
     torch.cuda.synchronize()
 
     # ---- timed region: K steps, L2 flushed between them, events around each step
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     clocks = ClockSampler(device)
     clocks.start()
     barrier(dist, device)
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush_l2(flush, drain, i)
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    step_ms = timed(graph.replay, args.steps, flush, drain)
     barrier(dist, device)
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     t_total = max_over_ranks(dist, sum(step_ms), device)
     ms_per_step = t_total / args.steps
     value = world * spec.rows * args.steps / (t_total / 1000.0)
 
-    # ---- per-kernel timing of the dominant kernel (stage 4) on the same stream
-    ld = (mv + 3) // 4 * 4
-    gws = ws  # the layer-step workspace is large enough for every stage call
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush_l2(flush, drain, i)
-        gev[i][0].record(stream)
-        Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], packed, wl["token_to_req"],
-                     wl["gate"], out, gws)
-        gev[i][1].record(stream)
-    torch.cuda.synchronize()
-    gqa_ms = statistics.mean(a.elapsed_time(b) for a, b in gev)
+    # ---- the dominant kernel (stage 4) alone, on the same stream
+    gqa_ms = gqa_kernel_ms(wl, gcfg, packed, out, ws, args.steps, flush, drain)
     step_bytes, gqa_bytes, parts = algorithmic_bytes(spec, wl, packed)
     peaks, peak_kind = load_peaks()
     hbm = float(peaks["hbm_gbs"])
@@ -471,39 +651,44 @@ def run_ours(args):
     step_gbs = step_bytes / (ms_per_step / 1000.0) / 1e9
 
     # ---- end to end: host buffers in, output back, through the same C-ABI call.
-    # The step's inputs sit in one pinned host buffer (256-byte aligned
-    # slots) and travel in one copy to one device buffer whose slices are the
-    # step's input tensors.
+    # The caller produces the step's inputs in one pinned host staging buffer
+    # (256-byte aligned slots); they travel in one copy to one device buffer
+    # whose slices are the step's input tensors.
     host_buf, dev_buf, t_e2e = pack_step_inputs(wl.t, STEP_INPUTS, device, pin=True)
     sargs_e2e = Q.step_args(t_e2e, packed, out, mv)
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(wl.t[k].numel() * wl.t[k].element_size() for k in STEP_INPUTS)
     d2h = out_host.numel() * out_host.element_size()
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush_l2(flush, drain, i)
-        eev[i][0].record(stream)
+
+    def e2e_step():
         dev_buf.copy_(host_buf, non_blocking=True)
         Q.layer_step(cfg, gcfg, sargs_e2e, ws)
         out_host.copy_(out, non_blocking=True)
-        eev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in eev), device) / args.steps
+
+    e2e_ms = max_over_ranks(dist, sum(timed(e2e_step, args.steps, flush, drain)), device) / args.steps
     e2e_value = world * spec.rows / (e2e_ms / 1000.0)
     if Q.check_errors() != 0:
         raise RuntimeError("device error word set during the timed steps")
 
     launches_per_step = Q.step_launches(cfg, gcfg, spec.rows, spec.reqs)
-    prefill = None
-    if rank == 0 and world == 1 and spec.name == "decode_batch" and not args.no_prefill:
-        prefill = prefill_report(device, 3, flush, drain)
-
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, rows_done, secs = oracle_sample(spec, wl, budget_s=args.ref_budget)
-        cpu = {"value": rate, "unit": unit_of(spec), "cores": cpu_threads(), "kind": "oracle",
-               "sample": f"{rows_done} rows (whole requests) of {spec.name}, {secs:.1f} s"}
+        rate, rows_done, secs, cores = oracle_sample(spec, wl, budget_s=args.ref_budget)
+        cpu = {"value": rate, "unit": unit_of(spec), "cores": cores, "kind": "oracle",
+               "sample": f"{rows_done} rows (whole requests) of {spec.name}, {secs:.1f} s; "
+                         f"cores = process CPU seconds / wall seconds"}
+    del wl, packed, out, ws, graph, host_buf, dev_buf, t_e2e, sargs, sargs_e2e
+    torch.cuda.empty_cache()
+
+    extra = None
+    if rank == 0 and world == 1 and spec.name == "decode_batch" and not args.no_extra:
+        fp8 = measure_fp8_peak(device)
+        bf16 = float(peaks["bf16_tflops"])
+        extra = {"fp8_peak": fp8,
+                 "prefill": prefill_report(device, 3, flush, drain, fp8, bf16,
+                                           not args.no_cpu_baseline),
+                 "long_decode": decode_report("long_decode", device, 10, 3, flush, drain, hbm),
+                 "mtp_mrope": mtp_report(device, 10, 3, flush, drain, hbm)}
 
     if rank == 0:
         line = {
@@ -512,14 +697,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3+bf16" if spec.index_dtype == W.DTYPE_E4M3 else "bf16",
             "data": "synthetic",
-            "config": {"workload": spec.name, "rows": spec.rows, "reqs": spec.reqs,
-                       "contexts": f"{min(spec.contexts)}..{max(spec.contexts)}",
-                       "indexer": f"{spec.n_heads}x128 {'e4m3' if spec.index_dtype else 'bf16'}"
-                                  f" r={spec.compress_ratio} topk={spec.token_topk}",
-                       "gqa": f"{spec.hq}q/{spec.hkv}kv x128 bf16 page {spec.page}",
-                       "parallelism": f"replicas x{world}",
-                       "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, then a "
-                             f"{DRAIN_BYTES >> 20} MiB read to evict the written lines)"},
+            "config": config_of(spec, world),
             "roofline": {"bound": "hbm", "kernel": "qsa sparse GQA (stage 4)",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm,
@@ -533,11 +711,13 @@ def run_ours(args):
                               "parts": parts},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": unit_of(spec), "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "inputs": "produced by the caller in one pinned staging buffer (no host "
+                              "repacking); one H2D copy, the C-ABI call, one D2H copy per step"},
             "gpu_launches": launches_per_step * args.steps,
             "launch": "CUDA graph of one qsa_layer_step call (value); direct calls (e2e)",
             "clocks": clk,
-            "prefill": prefill,
+            "other_workloads": extra,
         }
         print(json.dumps(line))
     if dist is not None:
@@ -553,8 +733,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_batch", choices=list(W.NAMED))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true",
-                    help="skip the chunked-prefill rows/s and index-logits measurement")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads (prefill, long decode, MTP draft) and the "
+                         "fp8 peak probe in the default run")
     ap.add_argument("--ref-budget", type=float, default=15.0)
     args = ap.parse_args()
     if args.impl == "reference":

@@ -220,7 +220,10 @@ qsa_status qsa_sparse_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv
  *    on the GPU race on it: order them on one stream or with events.
  *  - The first call on each device looks up the array's device address with
  *    that device current and caches it; make that first call before any
- *    stream capture.
+ *    stream capture.  cudaDeviceReset unloads the library's device code and
+ *    leaves that cached address stale: after resetting a device, do not call
+ *    this entry point on it again in the same process.
+ *  - Configuration checks are those of qsa_sparse_gqa.
  */
 #define QSA_NOALLOC_SCRATCH_BYTES (4u << 20)
 qsa_status qsa_sparse_gqa_noalloc(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
@@ -274,6 +277,29 @@ typedef struct qsa_step_args {
 qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg,
                           const qsa_step_args* args, int32_t skip_topk,
                           void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * qsa_mtp_steps -- the k layer steps of one multi-token-prediction draft, in
+ * order on one stream: steps[0] selects (stages 1-4, writing the packed
+ * buffer), steps[1 .. k-1] reuse that packed buffer unchanged (skip_topk:
+ * stage 1 still writes the ring and the compressed cache, stage 4 attends
+ * over the frozen selection).  Follows "vllm.models.qwen4_exp.nvidia.qsa",
+ * QSAIndexer.skip_topk (top-k computed at the first MTP step, reused by the
+ * later ones while the indexer cache keeps being updated) and the
+ * topk_indices_buffer shared across the steps.
+ *  steps  [k] step arguments; every step has the same rows, reqs and packed
+ *         pointer (the persistent selection buffer) and its own per-step
+ *         inputs and outputs (raw keys, positions, q, gate, out, ...)
+ *  k      1 .. QSA_MTP_MAX_STEPS
+ *  ws     one workspace of qsa_workspace_bytes() for these sizes, reused by
+ *         every step (the steps run in stream order)
+ * All k steps are validated before the first launch; on any error nothing is
+ * launched.  No host synchronisation: the whole draft can be captured into
+ * one CUDA graph.
+ */
+#define QSA_MTP_MAX_STEPS 16
+qsa_status qsa_mtp_steps(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa_step_args* steps,
+                         int32_t k, void* ws, size_t ws_bytes, void* stream);
 
 /* Scratch bytes needed by qsa_layer_step (and enough for every stage call)
  * for `rows` rows, `reqs` requests and V(p) <= max_visible.  The workspace

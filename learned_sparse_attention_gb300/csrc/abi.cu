@@ -66,18 +66,14 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int elem_bytes, long lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Multiprocessors of the current device (queried once per device).
-int sm_count() {
-  static int count[kMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
-  if (count[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-    count[dev] = n;
-  }
-  return count[dev];
-}
+// Set while qsa_mtp_steps validates all of its steps before it launches any
+// of them: the stage helpers then return right before their launches.
+thread_local bool t_validate_only = false;
+
+struct ValidateOnly {
+  ValidateOnly() { t_validate_only = true; }
+  ~ValidateOnly() { t_validate_only = false; }
+};
 
 bool pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -99,15 +95,6 @@ qsa_status check_cfg(const qsa_cfg* c) {
   if (c->state_size < c->compress_ratio) return QSA_ERR_SHAPE;
   if (!pow2(c->cpage) || c->cpage > 128) return QSA_ERR_UNSUPPORTED;
   if (c->max_position < 1) return QSA_ERR_INVALID_ARG;
-  return QSA_OK;
-}
-
-qsa_status check_gcfg(const qsa_gqa_cfg* g) {
-  if (g == nullptr) return QSA_ERR_INVALID_ARG;
-  if (g->head_dim != 128) return QSA_ERR_UNSUPPORTED;
-  if (g->num_kv_heads < 1 || g->num_q_heads != 8 * g->num_kv_heads) return QSA_ERR_UNSUPPORTED;
-  if (g->page_size < 16 || g->page_size % 16 != 0) return QSA_ERR_SHAPE;
-  if (g->num_blocks < 1) return QSA_ERR_SHAPE;
   return QSA_OK;
 }
 
@@ -146,7 +133,7 @@ struct GqaLayout {
 
 GqaLayout gqa_layout(const qsa_gqa_cfg* g, int rows, int packed_width) {
   GqaLayout L{};
-  L.splits = gqa_num_splits(rows, g->num_kv_heads, packed_width);
+  L.splits = gqa_num_splits(rows, g->num_kv_heads, packed_width, sm_count());
   if (L.splits == 1) return L;
   const long long slots = static_cast<long long>(L.splits) * rows * g->num_kv_heads;
   L.po = 0;
@@ -225,6 +212,7 @@ qsa_status do_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
   if (out_params != nullptr) *out_params = p;
+  if (t_validate_only) return QSA_OK;
   st = cuda_status(launch_compress(p, stream, /*pdl=*/false));
   if (st != QSA_OK || !commit_ring) return st;
   return cuda_status(launch_ring_commit(p, stream, /*pdl=*/true));
@@ -369,6 +357,7 @@ qsa_status do_topk(const qsa_cfg* cfg, const float* logits, int64_t ld, int32_t 
   p.tickets = tickets;
   p.tickets_per_row = tickets_per_row;
   p.sms = sm_count();
+  if (t_validate_only) return QSA_OK;
   return cuda_status(launch_topk(p, stream, pdl));
 }
 
@@ -413,6 +402,7 @@ qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
   }
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
+  if (t_validate_only) return QSA_OK;
   return cuda_status(launch_sparse_gqa(p, stream, pdl, !tickets_zeroed));
 }
 
@@ -445,6 +435,32 @@ bool step_layout(const qsa_cfg* c, const qsa_gqa_cfg* g, int rows, int reqs, int
 
 // Error word of the current device, for entry points defined in other files.
 unsigned long long* internal_error_word() { return error_word(); }
+
+// Multiprocessors of the current device (queried once per device).
+int sm_count() {
+  static int count[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+  if (count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    count[dev] = n;
+  }
+  return count[dev];
+}
+
+
+// Validation of the main-attention configuration, shared by every entry
+// point that runs stage 4.
+qsa_status check_gcfg(const qsa_gqa_cfg* g) {
+  if (g == nullptr) return QSA_ERR_INVALID_ARG;
+  if (g->head_dim != 128) return QSA_ERR_UNSUPPORTED;
+  if (g->num_kv_heads < 1 || g->num_q_heads != 8 * g->num_kv_heads) return QSA_ERR_UNSUPPORTED;
+  if (g->page_size < 16 || g->page_size % 16 != 0) return QSA_ERR_SHAPE;
+  if (g->num_blocks < 1) return QSA_ERR_SHAPE;
+  return QSA_OK;
+}
+
 
 }  // namespace qsa
 
@@ -543,7 +559,7 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
                    a->logical_positions, a->ccache, a->cpages, a->compressed_slots, a->rows,
                    a->reqs, s, /*commit_ring=*/false, &cp);
   if (st != QSA_OK) return st;
-  if (any_visible) {
+  if (any_visible && !t_validate_only) {
     st = launch_logits(cfg, lp, q_idx, a->rows, npad, chunks, groups, /*pdl=*/true, s);
     if (st != QSA_OK) return st;
   }
@@ -557,6 +573,28 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
   return do_gqa(gcfg, a->q, a->kv, a->block_table, a->bt_stride, a->packed, pw, a->token_to_req,
                 a->gate, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s, /*pdl=*/true,
                 /*tickets_zeroed=*/tickets != nullptr);
+}
+
+qsa_status qsa_mtp_steps(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa_step_args* steps,
+                         int32_t k, void* ws, size_t ws_bytes, void* stream) {
+  if (steps == nullptr || k < 1 || k > QSA_MTP_MAX_STEPS) return QSA_ERR_INVALID_ARG;
+  for (int s = 1; s < k; ++s) {
+    if (steps[s].rows != steps[0].rows || steps[s].reqs != steps[0].reqs ||
+        steps[s].packed != steps[0].packed)
+      return QSA_ERR_INVALID_ARG;
+  }
+  {
+    ValidateOnly guard;  // every step is checked before the first launch
+    for (int s = 0; s < k; ++s) {
+      const qsa_status st = qsa_layer_step(cfg, gcfg, &steps[s], s > 0, ws, ws_bytes, stream);
+      if (st != QSA_OK) return st;
+    }
+  }
+  for (int s = 0; s < k; ++s) {
+    const qsa_status st = qsa_layer_step(cfg, gcfg, &steps[s], s > 0, ws, ws_bytes, stream);
+    if (st != QSA_OK) return st;
+  }
+  return QSA_OK;
 }
 
 size_t qsa_workspace_bytes(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t rows,
@@ -576,7 +614,7 @@ int32_t qsa_step_launches(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, int32_t r
 
 int32_t qsa_gqa_splits(const qsa_gqa_cfg* gcfg, int32_t rows, int32_t packed_width) {
   if (check_gcfg(gcfg) != QSA_OK || rows <= 0 || packed_width < 2) return 0;
-  return gqa_num_splits(rows, gcfg->num_kv_heads, packed_width);
+  return gqa_num_splits(rows, gcfg->num_kv_heads, packed_width, sm_count());
 }
 
 const char* qsa_status_string(qsa_status s) {

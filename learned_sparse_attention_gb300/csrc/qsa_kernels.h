@@ -6,7 +6,14 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "qsa.h"
+
 namespace qsa {
+
+// Defined in abi.cu, shared by the entry points of other files.
+int sm_count();                                // multiprocessors of the current device
+qsa_status check_gcfg(const qsa_gqa_cfg* g);   // main-attention configuration checks
+unsigned long long* internal_error_word();     // device error word of the current device
 
 struct CompressParams {
   const uint16_t* projected_q;  // [rows, n_heads*128] bf16 or null
@@ -94,7 +101,8 @@ struct GqaParams {
   int rows, hq, hkv, page, num_blocks, splits;
   unsigned long long* err;
 };
-int gqa_num_splits(int rows, int hkv, int packed_width);
+// Split-KV factor for `rows` rows on a device with `sms` multiprocessors.
+int gqa_num_splits(int rows, int hkv, int packed_width, int sms);
 // zero_tickets: clear the merge tickets first (false when a preceding kernel
 // of the same step already did).
 cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,

@@ -431,10 +431,10 @@ __global__ void __launch_bounds__(256) gqa_merge_kernel(const GqaParams P) {
 
 }  // namespace
 
-// Split-KV count: about two CTAs per SM of a GB300 (152 SMs), and no CTA with
-// more than kMaxTiles 64-token tiles (one chunk of staged row ids, so that
-// the request's block-table row is read from shared memory).
-int gqa_num_splits(int rows, int hkv, int packed_width) {
+// Split-KV count: about two CTAs per SM, and no CTA with more than kMaxTiles
+// 64-token tiles (one chunk of staged row ids, so that the request's
+// block-table row is read from shared memory).
+int gqa_num_splits(int rows, int hkv, int packed_width, int sms) {
   const long long base = static_cast<long long>(rows) * hkv;
   if (base <= 0) return 1;
   const int max_tiles = (packed_width - 1 + kTile - 1) / kTile;
@@ -442,7 +442,7 @@ int gqa_num_splits(int rows, int hkv, int packed_width) {
   // as many splits as keep every (row, KV head, split) CTA resident in one
   // wave at two CTAs per SM (shared memory): a CTA's time grows with its
   // tokens, so shorter splits finish the launch sooner
-  long long s = 2 * 152 / base;
+  long long s = 2ll * sms / base;
   if (s > max_tiles) s = max_tiles;
   if (s > 64) s = 64;
   if (s < min_s) s = min_s;

@@ -23,7 +23,10 @@
 //    partial outputs and log-sum-exps before the merge reads them;
 //  - the first call on each device resolves the array's device address
 //    (cudaGetSymbolAddress, with that device current) and caches it; make
-//    that first call before any stream capture.
+//    that first call before any stream capture.  cudaDeviceReset unloads the
+//    library's device code, so the cached address is stale afterwards: a
+//    process that resets a device must not call this entry point on that
+//    device again.
 // Nothing here calls cudaMalloc, cudaFree or any allocating library routine.
 // This entry point has no counterpart on the pages the method comes from.
 #include <mutex>
@@ -31,10 +34,6 @@
 #include "qsa.h"
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
-
-namespace qsa {
-unsigned long long* internal_error_word();  // defined in abi.cu
-}
 
 namespace {
 
@@ -70,12 +69,8 @@ extern "C" qsa_status qsa_sparse_gqa_noalloc(const qsa_gqa_cfg* gcfg, const void
                                              int32_t packed_width, const int32_t* token_to_req,
                                              const void* gate, void* out, int32_t rows,
                                              void* stream) {
-  if (gcfg == nullptr) return QSA_ERR_INVALID_ARG;
-  if (gcfg->head_dim != 128) return QSA_ERR_UNSUPPORTED;
-  if (gcfg->num_kv_heads < 1 || gcfg->num_q_heads != 8 * gcfg->num_kv_heads)
-    return QSA_ERR_UNSUPPORTED;
-  if (gcfg->page_size < 16 || gcfg->page_size % 16 != 0 || gcfg->num_blocks < 1)
-    return QSA_ERR_SHAPE;
+  const qsa_status st = qsa::check_gcfg(gcfg);  // the checks qsa_sparse_gqa makes
+  if (st != QSA_OK) return st;
   if (rows < 0) return QSA_ERR_SHAPE;
   if (rows == 0) return QSA_OK;
   if (packed_width < 2 || bt_stride < 1) return QSA_ERR_SHAPE;
@@ -99,7 +94,7 @@ extern "C" qsa_status qsa_sparse_gqa_noalloc(const qsa_gqa_cfg* gcfg, const void
   p.hkv = gcfg->num_kv_heads;
   p.page = gcfg->page_size;
   p.num_blocks = gcfg->num_blocks;
-  p.splits = qsa::gqa_num_splits(rows, gcfg->num_kv_heads, packed_width);
+  p.splits = qsa::gqa_num_splits(rows, gcfg->num_kv_heads, packed_width, qsa::sm_count());
   if (p.splits > 1) {
     const size_t po = static_cast<size_t>(p.splits) * rows * p.hq * 128 * sizeof(float);
     const size_t pl = static_cast<size_t>(p.splits) * rows * p.hq * sizeof(float);

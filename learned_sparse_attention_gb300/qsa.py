@@ -79,6 +79,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qsa_topk": [P, P, ctypes.c_int64, I, P, P, I, P],
         "qsa_sparse_gqa": [P, P, P, P, I, P, I, P, P, P, I, P, Z, P],
         "qsa_layer_step": [P, P, P, I, P, Z, P],
+        "qsa_mtp_steps": [P, P, P, I, P, Z, P],
         "qsa_workspace_bytes": [P, P, I, I, I],
         "qsa_status_string": [I],
         "qsa_check_errors": [ctypes.POINTER(ctypes.c_int64)],
@@ -260,6 +261,20 @@ def layer_step(cfg, gcfg, args: QsaStepArgs, ws, skip_topk=False, stream=None):
                                1 if skip_topk else 0, _ptr(ws, torch.uint8), ws.numel(),
                                _stream(stream))
     _check("qsa_layer_step", st)
+
+
+MTP_MAX_STEPS = 16
+
+
+def mtp_steps(cfg, gcfg, steps, ws, stream=None):
+    """The k layer steps of one MTP draft (qsa_mtp_steps): steps[0] selects,
+    the later steps reuse its packed buffer.  `steps` is a list of
+    QsaStepArgs sharing rows, reqs and the packed buffer."""
+    k = len(steps)
+    arr = (QsaStepArgs * k)(*steps)
+    st = load().qsa_mtp_steps(ctypes.byref(cfg), ctypes.byref(gcfg), arr, k, _ptr(ws, torch.uint8),
+                              ws.numel(), _stream(stream))
+    _check("qsa_mtp_steps", st)
 
 
 def step_launches(cfg, gcfg, rows, reqs, skip_topk=False) -> int:

@@ -18,8 +18,12 @@ Workload recipe (all values seeded):
   gathers are not sequential;
 * RoPE cos/sin table: theta = 10000, fp32, [max_pos, rotary_dim] with cos
   in the first half and sin in the second;
-* the "peaked" long-context workload scales 1% of each request's token
-  positions by 8 in both the raw indexer key and the main-cache K row;
+* the "peaked" long-context workload picks a seeded 1% of each request's
+  token positions and scales by 8 the raw indexer key, the main-cache K row
+  and the compressed key of the group holding each of them (the prefix of
+  the compressed cache is a seeded fill, not stage 1 run over the history,
+  so the peak is placed there directly: the index scores of those groups
+  are then about 8 times the others');
 * the MTP/MRoPE workload gives each request one 1024-token image span laid
   out as a 32x32 (H, W) grid at fixed T; text tokens have T = H = W = t.
 """
@@ -260,33 +264,44 @@ def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0, with_caches: 
     # without the main KV cache (index-only studies) a one-block stand-in keeps the keys valid
     t["kv"] = _randn(gd, (n_kv_blocks if with_kv else 1, spec.hkv, spec.page, 2 * D), dev)
     cc = torch.randn((n_cpages, spec.cpage, 1, D), generator=gd, device=dev, dtype=torch.float32)
+    peaks = []  # per request: the peaked token positions
+    if spec.peak_frac > 0:
+        gp = np.random.default_rng([spec.seed, 99])
+        for req in range(reqs):
+            L = spec.contexts[req]
+            npk = max(1, int(round(spec.peak_frac * L)))
+            peaks.append(np.sort(gp.choice(L, size=npk, replace=False)))
+        # compressed keys of the groups holding a peaked token
+        for req, tok in enumerate(peaks):
+            grp = np.unique(tok // r)
+            flat = cblock_table[req, grp // spec.cpage].astype(np.int64) * spec.cpage + grp % spec.cpage
+            idx = torch.from_numpy(flat).to(dev)
+            ccf = cc.view(-1, D)
+            ccf[idx] = ccf[idx] * 8
     if spec.index_dtype == DTYPE_E4M3:
         t["ccache"] = cc.to(torch.float8_e4m3fn).view(torch.uint8)
     else:
         t["ccache"] = cc.to(torch.bfloat16)
 
     if spec.peak_frac > 0 and with_kv:
-        gp = np.random.default_rng([spec.seed, 99])
         for req in range(reqs):
+            tok = peaks[req]
             L = spec.contexts[req]
-            npk = max(1, int(round(spec.peak_frac * L)))
-            tok = gp.choice(L, size=npk, replace=False)
             blk = torch.from_numpy(block_table[req, tok // spec.page].astype(np.int64)).to(dev)
             off = torch.from_numpy((tok % spec.page).astype(np.int64)).to(dev)
             kv = t["kv"]
             kv[blk, :, off, :D] = kv[blk, :, off, :D] * 8
+            peaked = set(int(x) for x in tok)
             # this step's raw keys at peaked positions
-            first = qsl[req]
             for row in range(qsl[req], qsl[req + 1]):
-                if int(logical[row]) in set(int(x) for x in tok):
+                if int(logical[row]) in peaked:
                     t["raw_keys"][row] *= 8
             # ring entries holding peaked tokens
             firstpos = int(L - spec.rows_per_req[req])
             rb = int(ring_block_table[req, 0])
             for tt in range(max(0, firstpos - S), firstpos):
-                if tt in set(int(x) for x in tok):
+                if tt in peaked:
                     t["ring"][rb, tt % S] *= 8
-            del first
     t = {k: (v.to(dev) if v.device != dev else v) for k, v in t.items()}
     return Workload(spec, t, image_start)
 

@@ -140,3 +140,21 @@ def test_binding_rejects_host_tensors(lib):
     import torch
     with pytest.raises(ValueError):
         Q._ptr(torch.zeros(4), torch.float32, "x")
+
+
+def test_mtp_steps_rejects_bad_step_lists(lib):
+    g = Q.make_gqa_cfg(32, 4, 64, 1000)
+    a, b = Q.QsaStepArgs(), Q.QsaStepArgs()
+    a.rows = b.rows = 4
+    a.reqs = b.reqs = 1
+    a.packed, b.packed = 4096, 8192          # different packed buffers
+    arr = (Q.QsaStepArgs * 2)(a, b)
+    assert lib.qsa_mtp_steps(ctypes.byref(_cfg()), ctypes.byref(g), arr, 2, None, 0, None) == 1
+    b.rows = 5
+    b.packed = 4096
+    arr = (Q.QsaStepArgs * 2)(a, b)
+    assert lib.qsa_mtp_steps(ctypes.byref(_cfg()), ctypes.byref(g), arr, 2, None, 0, None) == 1
+    assert lib.qsa_mtp_steps(ctypes.byref(_cfg()), ctypes.byref(g), arr, 0, None, 0, None) == 1
+    assert lib.qsa_mtp_steps(ctypes.byref(_cfg()), ctypes.byref(g), None, 1, None, 0, None) == 1
+    big = (Q.QsaStepArgs * 17)(*([a] * 17))
+    assert lib.qsa_mtp_steps(ctypes.byref(_cfg()), ctypes.byref(g), big, 17, None, 0, None) == 1

@@ -253,8 +253,10 @@ def _full_chain(spec, wl, st, step, rows=None, packed_ref=None, skip=False):
             ok, ndiff = selection_ok(st.cfg, got_packed[row], opack, scores, p)
             assert ok, f"{spec.name} row {row}: selection differs beyond the tie window"
             if ndiff:
+                # a block inside the tie window went the other way: stage 4 is
+                # still checked, on the selection the GPU made
                 tie_rows += 1
-                continue
+                opack = got_packed[row]
         n = int(opack[-1])
         if st.kv is not None:
             want = O.sparse_gqa_row(st.q[row], st.kv, st.block_table[req], opack[:n], spec.page,
@@ -367,3 +369,137 @@ def test_full_size_invariants_decode_batch():
         assert toks.min() >= 0 and toks.max() <= p and len(np.unique(toks)) == n
         assert (pk[row, n:-1] == -1).all()
     assert np.isfinite(f64(step.out)).all()
+
+
+def test_full_size_mtp_step0_then_three_skip_topk_steps():
+    """The MTP verify workload with MRoPE as the pages run it: step 0 selects,
+    steps 1-3 reuse step 0's packed buffer (skip_topk) with fresh indexer
+    projections, raw keys, q and gate, while stage 1 keeps writing the
+    compressed cache and the ring.  Every step's caches are compared with
+    the oracle's own stage 1 over the same history, and the outputs of
+    sampled rows with the oracle's stage 4 on the reused selection.
+    Source: "vllm.models.qwen4_exp.nvidia.qsa", QSAIndexer.skip_topk (later
+    steps reuse the indices while the indexer cache is still updated)."""
+    spec = W.named_spec("mtp_mrope")
+    wl = W.make_workload(spec, device="cuda")
+    st = OracleState(wl, with_kv=False)
+    step = Step(wl).run()
+    assert Q.check_errors() == 0
+    rng = np.random.default_rng(3)
+    rows = np.sort(rng.choice(spec.rows, size=32, replace=False))
+    st.compress()
+    _full_chain(spec, wl, st, step, rows=rows)
+    packed0 = step.packed.cpu().numpy().copy()
+    slots = i64(wl["compressed_slots"])
+    sl = slots[slots >= 0]
+    for s in (1, 2, 3):
+        nxt = W.make_workload(spec, device="cuda", step=s, with_caches=False)
+        for k in ("projected_q", "raw_keys", "q", "gate"):
+            wl.t[k].copy_(nxt[k])
+            setattr(st, k, f64(nxt[k]).reshape(getattr(st, k).shape))
+        step.run(skip_topk=True)
+        assert Q.check_errors() == 0
+        st.compress()
+        np.testing.assert_array_equal(step.packed.cpu().numpy(), packed0)
+        rows = np.sort(rng.choice(spec.rows, size=32, replace=False))
+        _full_chain(spec, wl, st, step, rows=rows, packed_ref=packed0, skip=True)
+        ok, err = _close_idx(spec, f64(wl["ccache"]).reshape(-1, 128)[sl],
+                             st.ccache.reshape(-1, 128)[sl])
+        assert ok, f"step {s}: compressed keys {err}"
+        np.testing.assert_array_equal(f64(wl["ring"]).reshape(st.ring.shape), st.ring)
+        np.testing.assert_array_equal(i64(wl["ring_pos"]).reshape(st.ring_pos.shape), st.ring_pos)
+
+
+@pytest.mark.parametrize("rows,hkv", [(3, 4), (8, 8)])
+def test_split_merge_launch_matches_oracle(rows, hkv):
+    """Split-KV partials merged by a separate launch (the path taken when no
+    merge tickets are given, as in qsa_sparse_gqa_noalloc) against the
+    oracle's stage 4, with full, partial and empty selections."""
+    spec = W.small_spec("merge", seed=40 + rows, contexts=[5000 + 1000 * i for i in range(rows)],
+                        rows_per_req=[1] * rows, n_heads=8, index_dtype=BF, compress_ratio=4,
+                        token_topk=2048, hq=8 * hkv, hkv=hkv, page=64)
+    wl = W.make_workload(spec, device="cuda")
+    _, gcfg = cfgs(spec, wl)
+    assert Q.gqa_splits(gcfg, spec.rows, spec.packed_width) > 1
+    st = OracleState(wl, with_kv=False)
+    packed_np = random_packed(np.random.default_rng(rows), st.cfg, st.logical_positions,
+                              full_rows={0})
+    packed_np[-1, :] = -1
+    packed_np[-1, -1] = 0
+    out = torch.full_like(wl["q"], 3.0)
+    Q.sparse_gqa_noalloc(gcfg, wl["q"], wl["kv"], wl["block_table"],
+                         torch.from_numpy(packed_np).cuda(), wl["token_to_req"], wl["gate"], out)
+    torch.cuda.synchronize()
+    got = f64(out)
+    for row in range(spec.rows):
+        n = int(packed_np[row, -1])
+        req = int(st.token_to_req[row])
+        want = oracle_gqa_row(st.q[row], wl["kv"], st.block_table[req], packed_np[row, :n],
+                              spec.page, st.gate[row])
+        ok, err = close_bf16(got[row], want)
+        assert ok, f"row {row} (n={n}): max err {err:.3g}"
+    assert (got[-1] == 0).all()
+
+
+def test_mtp_steps_equals_step_by_step_and_oracle():
+    """qsa_mtp_steps (one call for a 4-step MTP draft: step 0 selects, steps
+    1-3 reuse the packed buffer) gives bit for bit what four layer_step
+    calls give, and both match the oracle step by step (caches after every
+    step, outputs on the reused selection)."""
+    from types import SimpleNamespace
+
+    spec = MID["mid_mrope_h8"]
+    wa = W.make_workload(spec, device="cuda")
+    wb = wa.clone()
+    st = OracleState(wa)
+    cfg, gcfg = cfgs(spec, wa)
+    mv = max_visible(spec)
+    k = 4
+    fresh = [W.make_workload(spec, device="cuda", step=s, with_caches=False) for s in range(k)]
+    names = ("projected_q", "raw_keys", "q", "gate")
+
+    def per_step(wl):
+        ts = []
+        for s in range(k):
+            t = dict(wl.t)
+            for n in names:
+                t[n] = fresh[s][n]
+            ts.append(t)
+        return ts
+
+    packed_a = torch.full((spec.rows, spec.packed_width), -7, dtype=torch.int32, device="cuda")
+    packed_b = packed_a.clone()
+    outs_a = [torch.full_like(wa["q"], 7.0) for _ in range(k)]
+    outs_b = [torch.full_like(wa["q"], 7.0) for _ in range(k)]
+    nbytes = Q.workspace_bytes(cfg, gcfg, spec.rows, spec.reqs, mv)
+    ws_a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ws_b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ta, tb = per_step(wa), per_step(wb)
+    Q.mtp_steps(cfg, gcfg, [Q.step_args(ta[s], packed_a, outs_a[s], mv) for s in range(k)], ws_a)
+    for s in range(k):
+        Q.layer_step(cfg, gcfg, Q.step_args(tb[s], packed_b, outs_b[s], mv), ws_b,
+                     skip_topk=s > 0)
+    torch.cuda.synchronize()
+    assert Q.check_errors() == 0
+    assert torch.equal(packed_a, packed_b)
+    for s in range(k):
+        assert torch.equal(outs_a[s].view(torch.int16), outs_b[s].view(torch.int16)), s
+    for n in ("ring", "ring_pos", "ccache"):
+        assert torch.equal(wa[n], wb[n]), n
+    # the oracle, step by step, on the same inputs
+    for s in range(k):
+        for n in names:
+            setattr(st, n, f64(fresh[s][n]).reshape(getattr(st, n).shape))
+        st.compress()  # the oracle's caches now hold step s's stage 1
+        view = SimpleNamespace(packed=packed_a, out=outs_a[s], wl=wa)
+        if s == 0:
+            _full_chain(spec, wa, st, view)  # selection from step 0's caches
+            packed0 = packed_a.cpu().numpy().copy()
+        else:
+            _full_chain(spec, wa, st, view, packed_ref=packed0, skip=True)
+    np.testing.assert_array_equal(f64(wa["ring"]).reshape(st.ring.shape), st.ring)
+    np.testing.assert_array_equal(i64(wa["ring_pos"]).reshape(st.ring_pos.shape), st.ring_pos)
+    sl = i64(wa["compressed_slots"])
+    sl = sl[sl >= 0]
+    ok, err = _close_idx(spec, f64(wa["ccache"]).reshape(-1, 128)[sl], st.ccache.reshape(-1, 128)[sl])
+    assert ok, err

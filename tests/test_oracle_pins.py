@@ -378,3 +378,165 @@ def test_sparse_gqa_single_token_returns_its_value():
     out = O.sparse_gqa_row(q, kv, bt, [77], 16)
     v = kv[bt[77 // 16], :, 77 % 16, 128:]
     np.testing.assert_array_equal(out, np.repeat(v, 4, axis=0))
+
+
+# --------------------------------------------------------------------------
+# Stage-1 position sourcing, the compressed-page map and the query prep,
+# each pinned against an independent restatement: RoPE as a complex
+# rotation with the hand-derived [8, 12, 12] component table, the norm by
+# torch's rms_norm, and values worked out by hand.
+# --------------------------------------------------------------------------
+
+def _golden_components():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "mrope_components_8_12_12.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    table = {int(i): "THW".index(c) for i, c in rows}
+    return [table[i] for i in range(32)]
+
+
+def _rope_complex(x, pos3, comps):
+    """NeoX RoPE as a complex rotation: frequency i turns x[i] + 1j * x[i + 32]
+    by pos3[comps[i]] * 10000**(-i / 32); dims 64.. pass through."""
+    x = np.array(x, dtype=np.float64)
+    out = x.copy()
+    ang = np.array([pos3[comps[i]] for i in range(32)], dtype=np.float64) * \
+        10000.0 ** (-np.arange(32) / 32.0)
+    z = (x[..., :32] + 1j * x[..., 32:64]) * np.exp(1j * ang)
+    out[..., :32] = z.real
+    out[..., 32:64] = z.imag
+    return out
+
+
+def _norm(x, w, eps):
+    t = torch.from_numpy(np.asarray(x, dtype=np.float64))
+    return F.rms_norm(t, (t.shape[-1],), torch.from_numpy(1.0 + np.asarray(w, np.float64)),
+                      eps=eps).numpy()
+
+
+def _within_one_bf16_step(got, want):
+    """got is a bf16 value and want an unrounded value: got must be one of
+    the two bf16 neighbours of want (the rounding of an fp64 quantity that
+    two evaluation orders agree on to ~1e-15)."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(want))[1] - 8)
+    assert (np.abs(got - want) <= ulp).all(), np.abs(got - want).max()
+    # and nearly always the nearest one
+    assert (got == O.round_bf16(want)).mean() >= 0.99
+
+
+def _image_positions(n_tokens, img_start, side):
+    """3-D positions of tokens 0..n-1 with one side x side image span at
+    img_start (T fixed at the span start, H and W the grid coordinates)."""
+    pos = np.stack([np.arange(n_tokens)] * 3, axis=1).astype(np.int64)
+    span = side * side
+    for t in range(img_start, min(n_tokens, img_start + span)):
+        j = t - img_start
+        pos[t] = (img_start, img_start + j // side, img_start + j % side)
+    return pos
+
+
+@pytest.mark.parametrize("in_step", [1, 2, 3, 4, 6])
+def test_compress_mrope_key_takes_first_member_position_from_step_or_ring(in_step):
+    """MRoPE (reading R11): the compressed key of group g is rotated at the
+    3-D position of its FIRST token g*r, read from this step's positions
+    when that token is in the step, else from the ring's position cache at
+    slot (g*r) mod S.  The tokens of the group sit inside an image span, so
+    every member has a different (H, W): taking the last member's
+    position, or reading the ring at a neighbouring slot, changes the key.
+    Source: "indexer_qsa.py", apply_qsa_rope (rotation at the given
+    positions); "vllm.models.qwen4_exp.nvidia.qsa", QSAIndexer.forward,
+    unfused path (RoPE of the pooled key at the group's first positions,
+    qsa_store_cache_rows of the rope positions into the ring)."""
+    r, S, sec = 4, 8, (8, 12, 12)
+    cfg = _cfg(compress_ratio=r, state_size=S, mrope_section=sec)
+    cs = _table()
+    comps = _golden_components()
+    p = 43                                    # completes group 10: tokens 40..43
+    g = (p + 1) // r - 1
+    pos3 = _image_positions(p + 1, img_start=20, side=6)
+    assert len({tuple(pos3[t]) for t in range(40, 44)}) == 4
+    hist = RNG.standard_normal((p + 1, 128))
+    wk = RNG.standard_normal(128) * 0.1
+    start = p - in_step + 1
+    rows = in_step
+    ring = np.zeros((2, S, 128))
+    ring_pos = np.full((2, S, 3), -1, dtype=np.int64)
+    for t in range(max(0, start - S), start):
+        ring[1, t % S] = hist[t]
+        ring_pos[1, t % S] = pos3[t]
+    ccache = np.zeros((8, cfg.cpage, 128))
+    slots = np.full(rows, -1)
+    slots[-1] = 2 * cfg.cpage + 3
+    O.compress_stage(cfg, projected_q=None, raw_keys=hist[start:], positions=pos3[start:],
+                     cos_sin=cs, q_norm_w=np.zeros(128), k_norm_w=wk, ring=ring,
+                     ring_pos=ring_pos, ring_block_table=np.array([[1]]),
+                     token_to_req=np.zeros(rows, dtype=int), query_start_loc=np.array([0, rows]),
+                     logical_positions=np.arange(start, p + 1), ccache=ccache,
+                     compressed_slots=slots)
+    want = _rope_complex(_norm(hist[g * r:g * r + r].mean(0), wk, cfg.eps), pos3[g * r], comps)
+    _within_one_bf16_step(ccache[2, 3], want)
+    # the other members' positions give a different key
+    for t in range(g * r + 1, p + 1):
+        other = _rope_complex(_norm(hist[g * r:g * r + r].mean(0), wk, cfg.eps), pos3[t], comps)
+        assert np.abs(O.round_bf16(other) - ccache[2, 3]).max() > 1e-2
+    # the ring now holds this step's raw keys and positions at t mod S
+    for t in range(start, p + 1):
+        np.testing.assert_array_equal(ring[1, t % S], hist[t])
+        np.testing.assert_array_equal(ring_pos[1, t % S], pos3[t])
+
+
+def test_gather_compressed_keys_follows_the_page_table():
+    """Reading R9: compressed key c of a request is entry c mod cpage of
+    physical page cblock_row[c // cpage] (the logits column count
+    cdiv(max_len, block) * cdiv(block, ratio) in
+    "vllm.models.qwen4_exp.nvidia.qsa", Qwen4ExpQSAAttention._run_qsa:
+    one compressed page per KV block).  A cache whose key c holds the value
+    c (plus d / 1000 in dim d) under a permuted page table must come back as
+    0, 1, ..., V-1 in order."""
+    cfg = _cfg(cpage=4)
+    cblock_row = np.array([5, 2, 7, 0])
+    V = 13
+    ccache = np.full((8, 4, 128), -1.0)
+    for c in range(16):
+        ccache[cblock_row[c // 4], c % 4] = c + np.arange(128) / 1000.0
+    got = O.gather_compressed_keys(cfg, ccache, cblock_row, V)
+    assert got.shape == (V, 128)
+    np.testing.assert_array_equal(got, np.arange(V)[:, None] + np.arange(128)[None, :] / 1000.0)
+
+
+def test_prep_query_hand_worked_two_heads_mrope():
+    """Query prep of one row worked out by hand: per head (reshape
+    [H * D] -> [H, D]) a Gemma RMSNorm with scale 1 + w, THEN NeoX RoPE with
+    MRoPE [8, 12, 12] (frequency 0 rotates at T, frequency 1 at H), then one
+    bf16 rounding.  Source: "vllm.models.qwen4_exp.nvidia.qsa",
+    QSAIndexer.forward, unfused path (gemma_rmsnorm(q) -> apply_qsa_rope ->
+    cast); "indexer_qsa.py", apply_qsa_rope."""
+    cfg = _cfg(n_heads=2, eps=0.0, mrope_section=(8, 12, 12))
+    cs = _table()
+    x = np.zeros(256)
+    x[0], x[32] = 3.0, 4.0                        # head 0: pair of frequency 0
+    x[128 + 1], x[128 + 33], x[128 + 100] = 1.0, -2.0, 2.0  # head 1: frequency 1 + a tail dim
+    w = np.zeros(128)
+    w[0], w[32], w[1], w[33], w[100] = 0.5, -0.25, 0.1, 0.3, -0.5
+    T, H, Wd = 7, 300, 1000
+    got = O.prep_query(cfg, x, (T, H, Wd), cs, w)
+    want = np.zeros((2, 128))
+    # head 0: mean square 25/128, so 1/rms = sqrt(128)/5; angle T * 1
+    a0 = 3.0 * math.sqrt(128) / 5 * 1.5
+    b0 = 4.0 * math.sqrt(128) / 5 * 0.75
+    want[0, 0] = a0 * math.cos(T) - b0 * math.sin(T)
+    want[0, 32] = b0 * math.cos(T) + a0 * math.sin(T)
+    # head 1: mean square 9/128, so 1/rms = sqrt(128)/3; angle H * 10000^(-1/32)
+    k = math.sqrt(128) / 3
+    a1, b1 = 1.0 * k * 1.1, -2.0 * k * 1.3
+    th = H * 10000.0 ** (-1.0 / 32.0)
+    want[1, 1] = a1 * math.cos(th) - b1 * math.sin(th)
+    want[1, 33] = b1 * math.cos(th) + a1 * math.sin(th)
+    want[1, 100] = 2.0 * k * 0.5
+    _within_one_bf16_step(got, want)
+    # norm-then-rotate differs from rotate-then-norm for these weights
+    swapped = O.gemma_rmsnorm(O.rope_neox(x.reshape(2, 128), (T, H, Wd), cs, 64, (8, 12, 12)),
+                              w, 0.0)
+    assert np.abs(O.round_bf16(swapped) - got).max() > 0.1
