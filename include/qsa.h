@@ -85,7 +85,8 @@ typedef struct qsa_cfg {
  * Qwen4ExpQSAImpl: num_heads, head_size, num_kv_heads; paged KV block size a
  * multiple of 16). */
 typedef struct qsa_gqa_cfg {
-  int32_t num_q_heads;   /* Hq, a multiple of Hkv with Hq / Hkv == 8 */
+  int32_t num_q_heads;   /* Hq, a multiple of Hkv; the group Hq / Hkv is 1..8 or 16
+                            (other groups: QSA_ERR_UNSUPPORTED) */
   int32_t num_kv_heads;  /* Hkv */
   int32_t head_dim;      /* must be 128 */
   int32_t page_size;     /* tokens per KV block, a multiple of 16 */
@@ -192,6 +193,7 @@ qsa_status qsa_topk(const qsa_cfg* cfg, const float* logits, int64_t ld,
  *         block_table[q, t / page_size], offset t % page_size
  *  packed [rows, packed_width] int32; token_to_req [rows]
  *  gate   [rows, Hq, D] bf16 or NULL;  out [rows, Hq, D] bf16
+ *  (query head h of a row reads KV head h / (Hq / Hkv))
  *  ws     scratch (split-KV partials and their merge tickets),
  *         qsa_workspace_bytes() bytes
  */

@@ -137,8 +137,9 @@ GqaLayout gqa_layout(const qsa_gqa_cfg* g, int rows, int packed_width) {
   if (L.splits == 1) return L;
   const long long slots = static_cast<long long>(L.splits) * rows * g->num_kv_heads;
   L.po = 0;
-  L.pl = align256(static_cast<size_t>(slots) * 8 * 128 * sizeof(float));
-  L.tickets = L.pl + align256(static_cast<size_t>(slots) * 8 * sizeof(float));
+  const int group = g->num_q_heads / g->num_kv_heads;
+  L.pl = align256(static_cast<size_t>(slots) * group * 128 * sizeof(float));
+  L.tickets = L.pl + align256(static_cast<size_t>(slots) * group * sizeof(float));
   L.total = L.tickets + align256(static_cast<size_t>(rows) * g->num_kv_heads * sizeof(unsigned));
   return L;
 }
@@ -388,6 +389,7 @@ qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
   p.rows = rows;
   p.hq = gcfg->num_q_heads;
   p.hkv = gcfg->num_kv_heads;
+  p.group = gcfg->num_q_heads / gcfg->num_kv_heads;
   p.page = gcfg->page_size;
   p.num_blocks = gcfg->num_blocks;
   const GqaLayout G = gqa_layout(gcfg, rows, packed_width);
@@ -455,7 +457,11 @@ int sm_count() {
 qsa_status check_gcfg(const qsa_gqa_cfg* g) {
   if (g == nullptr) return QSA_ERR_INVALID_ARG;
   if (g->head_dim != 128) return QSA_ERR_UNSUPPORTED;
-  if (g->num_kv_heads < 1 || g->num_q_heads != 8 * g->num_kv_heads) return QSA_ERR_UNSUPPORTED;
+  if (g->num_kv_heads < 1 || g->num_q_heads < g->num_kv_heads ||
+      g->num_q_heads % g->num_kv_heads != 0)
+    return QSA_ERR_SHAPE;
+  const int group = g->num_q_heads / g->num_kv_heads;  // query heads per KV head
+  if (group > 8 && group != 16) return QSA_ERR_UNSUPPORTED;
   if (g->page_size < 16 || g->page_size % 16 != 0) return QSA_ERR_SHAPE;
   if (g->num_blocks < 1) return QSA_ERR_SHAPE;
   return QSA_OK;

@@ -98,7 +98,7 @@ struct GqaParams {
   float* part_lse;         // [splits, rows, Hq]
   unsigned* counters;      // [rows, Hkv] merge tickets, or null for a separate merge launch
   int bt_stride, packed_width;
-  int rows, hq, hkv, page, num_blocks, splits;
+  int rows, hq, hkv, group, page, num_blocks, splits;  // group = hq / hkv: 1..8 or 16
   unsigned long long* err;
 };
 // Split-KV factor for `rows` rows on a device with `sms` multiprocessors.

@@ -14,8 +14,10 @@
 // split), 4 warps.  Each warp owns 16 tokens of every 64-token tile and runs
 // its own 3-stage cp.async ring over them (16-byte copies, one token row per
 // warp instruction, XOR-swizzled so ldmatrix is conflict-free).  The GQA
-// group of 8 query heads is the N = 8 side of m16n8k16 MMAs with the tokens
-// on M, so no lane is padding:
+// group of query heads is the N = 8 side of m16n8k16 MMAs with the tokens
+// on M (groups of 1 to 8 heads fill one column block, zero queries in the
+// unused columns; groups of 16 take two blocks that share every K and V
+// fragment):
 //   S^T[16 tok x 8 heads] = K[16 x 128] . Q^T          (8 k-steps)
 //   O^T[128 dims x 8 heads] += V^T[128 x 16] . P^T       (8 m-tiles)
 // P^T comes from the S^T accumulator with one movmatrix transpose per 8x8
@@ -38,7 +40,6 @@
 namespace qsa {
 namespace {
 
-constexpr int kG = 8;          // query heads per KV head
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRidBatch = 8;  // KV row ids resolved per thread per batch
@@ -110,6 +111,8 @@ __device__ __forceinline__ uint32_t kv_row_id(const GqaParams& P, int off, int p
   return (static_cast<uint32_t>(pid) * P.hkv + kvh) * static_cast<uint32_t>(P.page) + off;
 }
 
+// NB: column blocks of 8 query heads (1 for groups of 1-8, 2 for 16).
+template <int NB>
 __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_vmask[kWarps][kStages];
@@ -126,17 +129,23 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   const int g = lane >> 2, t = lane & 3;
   const int Wcols = P.packed_width - 1;
 
+  const int G = P.group;
   griddep_launch_dependents();
   const int req = P.token_to_req[row];
   const int32_t* prow = P.packed + static_cast<long long>(row) * P.packed_width;
-  // Q^T fragments (B operand of S^T = K.Q^T): head kvh*8 + g, 2 dims per
-  // register; a caller input, loaded before waiting for the top-k kernel.
-  const uint16_t* qh = P.q + (static_cast<long long>(row) * P.hq + kvh * kG + g) * 128;
-  uint32_t qb[8][2];
+  // Q^T fragments (B operand of S^T = K.Q^T): head kvh * G + 8 nb + g (zero
+  // past the group), 2 dims per register; a caller input, loaded before
+  // waiting for the top-k kernel.
+  uint32_t qb[NB][8][2];
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    qb[kk][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t);
-    qb[kk][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t);
+  for (int nb = 0; nb < NB; ++nb) {
+    const int hl = nb * 8 + g;
+    const uint16_t* qh = P.q + (static_cast<long long>(row) * P.hq + kvh * G + min(hl, G - 1)) * 128;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      qb[nb][kk][0] = hl < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t) : 0u;
+      qb[nb][kk][1] = hl < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t) : 0u;
+    }
   }
   // The request's block-table row (a caller input) is copied before the
   // wait into the last pipeline stage of all warps (contiguous, and not
@@ -156,12 +165,16 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
         if (i0 + u * kThreads < P.bt_stride) s_bt[i0 + u * kThreads] = v[u];
     }
   }
-  // the epilogue's (head, 8 dims) of this thread and their gate (a caller input)
-  const int h = threadIdx.x >> 4;          // 0..7
-  const int d0 = (threadIdx.x & 15) * 8;   // 8 dims per thread
-  const int hq = kvh * kG + h;
-  const long long obase = (static_cast<long long>(row) * P.hq + hq) * 128 + d0;
-  const uint4 gate8 = load_gate8(P, obase);
+  // the epilogue's items of this thread (item tid + 128 nb: head item / 16 of
+  // the group, 8 dims) and their gate (a caller input)
+  const int d0 = (threadIdx.x & 15) * 8;   // 8 dims per item
+  uint4 gate8[NB];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    const int hh = (threadIdx.x + kThreads * nb) >> 4;
+    gate8[nb] = hh < G ? load_gate8(P, (static_cast<long long>(row) * P.hq + kvh * G + hh) * 128 + d0)
+                       : make_uint4(0u, 0u, 0u, 0u);
+  }
   griddep_wait();  // the packed selection (and merge tickets) are written
   // Without split-KV the CTA's range starts at token 0 whatever the count,
   // so its first entries (kFirst per thread, up to kFirst * kThreads tokens)
@@ -192,10 +205,15 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   const bool sbt = bt_fits && ntok <= kMaxTok;
   __syncthreads();  // the staged block-table row is complete
 
-  float o[8][4];
+  float o[NB][8][4];
+  float m0[NB], m1[NB], l0[NB], l1[NB];
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[nb][mt][0] = o[nb][mt][1] = o[nb][mt][2] = o[nb][mt][3] = 0.f;
+    m0[nb] = m1[nb] = -INFINITY;
+    l0[nb] = l1[nb] = 0.f;
+  }
   const float sl2 = 0.08838834764831845f * kLog2e;  // 128^-0.5 * log2(e)
   bool bad = false;
 
@@ -284,66 +302,75 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
       const uint8_t* sK = smem + (stage * kWarps + warp) * kSlab;
       const uint8_t* sV = sK + 4096;
       // S^T = K.Q^T over 8 K-steps, split over four accumulators so that the
-      // MMAs form four dependent chains of two instead of one of eight
-      float sa[4][4];
+      // MMAs form four dependent chains of two instead of one of eight (each
+      // K fragment feeds every column block)
+      float sa[NB][4][4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) sa[c][0] = sa[c][1] = sa[c][2] = sa[c][3] = 0.f;
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sa[nb][c][0] = sa[nb][c][1] = sa[nb][c][2] = sa[nb][c][3] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         uint32_t a[4];
         const int rl = lane & 15;
         const int ch = 2 * kk + (lane >> 4);
         ldmatrix_x4(a, sK + rl * 256 + ((ch ^ (rl & 7)) << 4));
-        mma_bf16_16816(sa[kk & 3], a, qb[kk][0], qb[kk][1]);
-      }
-      float s[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[e] = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
+        for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sa[nb][kk & 3], a, qb[nb][kk][0], qb[nb][kk][1]);
+      }
       const uint32_t vm = s_vmask[warp][stage];
       const bool v0 = (vm >> g) & 1u, v1 = (vm >> (g + 8)) & 1u;
-      const float x0 = v0 ? s[0] * sl2 : -INFINITY;  // token g,   head 2t
-      const float x1 = v0 ? s[1] * sl2 : -INFINITY;  // token g,   head 2t+1
-      const float x2 = v1 ? s[2] * sl2 : -INFINITY;  // token g+8, head 2t
-      const float x3 = v1 ? s[3] * sl2 : -INFINITY;  // token g+8, head 2t+1
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+      uint32_t pb[NB][2];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float b0 = mn0 == -INFINITY ? 0.f : mn0;
-      const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float p0 = exp2f(x0 - b0), p1 = exp2f(x1 - b1);
-      const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
-      // the running sums and the accumulator need rescaling only where a
-      // running max grew (the factor is exactly 1 elsewhere): skipped when no
-      // lane's max moved
-      if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-        const float al0 = exp2f(m0 - b0), al1 = exp2f(m1 - b1);
-        l0 *= al0;
-        l1 *= al1;
+      for (int nb = 0; nb < NB; ++nb) {
+        float sc[4];
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][0] *= al0;
-          o[mt][1] *= al1;
-          o[mt][2] *= al0;
-          o[mt][3] *= al1;
+        for (int e = 0; e < 4; ++e) sc[e] = (sa[nb][0][e] + sa[nb][1][e]) + (sa[nb][2][e] + sa[nb][3][e]);
+        const float x0 = v0 ? sc[0] * sl2 : -INFINITY;  // token g,   head 2t
+        const float x1 = v0 ? sc[1] * sl2 : -INFINITY;  // token g,   head 2t+1
+        const float x2 = v1 ? sc[2] * sl2 : -INFINITY;  // token g+8, head 2t
+        const float x3 = v1 ? sc[3] * sl2 : -INFINITY;  // token g+8, head 2t+1
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
+        const float mn0 = fmaxf(m0[nb], mx0), mn1 = fmaxf(m1[nb], mx1);
+        const float b0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float b1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float p0 = exp2f(x0 - b0), p1 = exp2f(x1 - b1);
+        const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
+        // the running sums and the accumulator need rescaling only where a
+        // running max grew (the factor is exactly 1 elsewhere): skipped when
+        // no lane's max moved
+        if (__any_sync(0xffffffffu, mn0 != m0[nb] || mn1 != m1[nb])) {
+          const float al0 = exp2f(m0[nb] - b0), al1 = exp2f(m1[nb] - b1);
+          l0[nb] *= al0;
+          l1[nb] *= al1;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[nb][mt][0] *= al0;
+            o[nb][mt][1] *= al1;
+            o[nb][mt][2] *= al0;
+            o[nb][mt][3] *= al1;
+          }
+        }
+        l0[nb] += p0 + p2;
+        l1[nb] += p1 + p3;
+        m0[nb] = mn0;
+        m1[nb] = mn1;
+        pb[nb][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+        pb[nb][1] = movmatrix_trans(pack_bf16x2(p2, p3));
       }
-      l0 += p0 + p2;
-      l1 += p1 + p3;
-      m0 = mn0;
-      m1 = mn1;
-      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t a[4];
         const int tk = (lane & 7) + ((lane >> 4) << 3);
         const int ch = 2 * mt + ((lane >> 3) & 1);
         ldmatrix_x4_trans(a, sV + tk * 256 + ((ch ^ (tk & 7)) << 4));
-        mma_bf16_16816(o[mt], a, pb0, pb1);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[nb][mt], a, pb[nb][0], pb[nb][1]);
       }
       __syncwarp();
       const int nxt = it + kStages - 1;
@@ -354,55 +381,67 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   }
   if (bad) flag_error(P.err);
 
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
   __syncthreads();  // pipeline buffers are free from here on
-  float* cm = reinterpret_cast<float*>(smem);   // [warps][8] max
-  float* cl = cm + kWarps * kG;                 // [warps][8] sum
-  float* co = cl + kWarps * kG;                 // [warps][8 heads][128 dims]
-  if (lane < 4) {
-    cm[warp * kG + 2 * t] = m0;
-    cm[warp * kG + 2 * t + 1] = m1;
-    cl[warp * kG + 2 * t] = l0;
-    cl[warp * kG + 2 * t + 1] = l1;
-  }
+  float* cm = reinterpret_cast<float*>(smem);   // [warps][8 NB] max
+  float* cl = cm + kWarps * 8 * NB;             // [warps][8 NB] sum
+  float* co = cl + kWarps * 8 * NB;             // [warps][8 NB heads][128 dims]
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int d = 16 * mt + g;
-    co[(warp * kG + 2 * t) * 128 + d] = o[mt][0];
-    co[(warp * kG + 2 * t + 1) * 128 + d] = o[mt][1];
-    co[(warp * kG + 2 * t) * 128 + d + 8] = o[mt][2];
-    co[(warp * kG + 2 * t + 1) * 128 + d + 8] = o[mt][3];
+  for (int nb = 0; nb < NB; ++nb) {
+    float la = l0[nb], lb = l1[nb];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      la += __shfl_xor_sync(0xffffffffu, la, off);
+      lb += __shfl_xor_sync(0xffffffffu, lb, off);
+    }
+    const int hb = warp * 8 * NB + nb * 8;
+    if (lane < 4) {
+      cm[hb + 2 * t] = m0[nb];
+      cm[hb + 2 * t + 1] = m1[nb];
+      cl[hb + 2 * t] = la;
+      cl[hb + 2 * t + 1] = lb;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d = 16 * mt + g;
+      co[(hb + 2 * t) * 128 + d] = o[nb][mt][0];
+      co[(hb + 2 * t + 1) * 128 + d] = o[nb][mt][1];
+      co[(hb + 2 * t) * 128 + d + 8] = o[nb][mt][2];
+      co[(hb + 2 * t + 1) * 128 + d + 8] = o[nb][mt][3];
+    }
   }
   __syncthreads();
 
-  float M = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * kG + h]);
-  float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int nb = 0; nb < NB; ++nb) {
+    const int hh = (threadIdx.x + kThreads * nb) >> 4;  // head within the group
+    if (hh >= G) continue;
+    float M = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const float mw = cm[w * kG + h];
-    const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
-    L += cl[w * kG + h] * wt;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * 8 * NB + hh]);
+    float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += co[(w * kG + h) * 128 + d0 + e] * wt;
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = cm[w * 8 * NB + hh];
+      const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      L += cl[w * 8 * NB + hh] * wt;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += co[(w * 8 * NB + hh) * 128 + d0 + e] * wt;
+    }
+    const float inv = L > 0.f ? 1.0f / L : 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= inv;
+    const int hq = kvh * G + hh;
+    if (P.splits == 1) {
+      store_out8(P, (static_cast<long long>(row) * P.hq + hq) * 128 + d0, acc, gate8[nb]);
+      continue;
+    }
+    const long long pb = (static_cast<long long>(split) * P.rows + row) * P.hq + hq;
+    float4* po = reinterpret_cast<float4*>(P.part_o + pb * 128 + d0);
+    po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if ((threadIdx.x & 15) == 0) P.part_lse[pb] = L > 0.f ? M + __log2f(L) : -INFINITY;
   }
-  const float inv = L > 0.f ? 1.0f / L : 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] *= inv;
-  if (P.splits == 1) {
-    store_out8(P, obase, acc, gate8);
-    return;
-  }
-  const long long pb = (static_cast<long long>(split) * P.rows + row) * P.hq + hq;
-  float4* po = reinterpret_cast<float4*>(P.part_o + pb * 128 + d0);
-  po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  if ((threadIdx.x & 15) == 0) P.part_lse[pb] = L > 0.f ? M + __log2f(L) : -INFINITY;
+  if (P.splits == 1) return;
   if (P.counters == nullptr) return;  // a separate merge launch follows
   // The last split of this (row, KV head) to finish merges them all.
   __threadfence();
@@ -414,7 +453,11 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  merge8(P, row, hq, d0, gate8);
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    const int hh = (threadIdx.x + kThreads * nb) >> 4;
+    if (hh < G) merge8(P, row, kvh * G + hh, d0, gate8[nb]);
+  }
   if (threadIdx.x == 0) P.counters[pair] = 0u;  // ready for the next launch
 }
 
@@ -455,22 +498,25 @@ cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
   if (p.rows == 0) return cudaSuccess;
   if (static_cast<long long>(p.num_blocks) * p.hkv * p.page >= static_cast<long long>(kBadRow))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
+  if (p.group < 1 || (p.group > 8 && p.group != 16)) return cudaErrorInvalidValue;
+  auto kern = p.group <= 8 ? gqa_kernel<1> : gqa_kernel<2>;
+  const int ki = p.group <= 8 ? 0 : 1;
+  static bool attr_set[2][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (dev < 0 || dev >= 64 || !attr_set[ki][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gqa_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[ki][dev] = true;
   }
   if (p.splits > 1 && p.counters != nullptr && zero_tickets) {
     cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(unsigned) * p.rows * p.hkv, stream);
     if (e != cudaSuccess) return e;
     pdl = false;  // a memset node sits between this kernel and its predecessor
   }
-  cudaError_t e = launch_kernel(gqa_kernel, dim3(p.rows * p.hkv, p.splits), dim3(kThreads), kSmem,
+  cudaError_t e = launch_kernel(kern, dim3(p.rows * p.hkv, p.splits), dim3(kThreads), kSmem,
                                 stream, pdl, p);
   if (e != cudaSuccess || p.splits == 1 || p.counters != nullptr) return e;
   return launch_kernel(gqa_merge_kernel, dim3(p.rows), dim3(256), 0, stream, true, p);

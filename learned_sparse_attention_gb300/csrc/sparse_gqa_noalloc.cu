@@ -92,6 +92,7 @@ extern "C" qsa_status qsa_sparse_gqa_noalloc(const qsa_gqa_cfg* gcfg, const void
   p.rows = rows;
   p.hq = gcfg->num_q_heads;
   p.hkv = gcfg->num_kv_heads;
+  p.group = gcfg->num_q_heads / gcfg->num_kv_heads;
   p.page = gcfg->page_size;
   p.num_blocks = gcfg->num_blocks;
   p.splits = qsa::gqa_num_splits(rows, gcfg->num_kv_heads, packed_width, qsa::sm_count());

@@ -98,10 +98,23 @@ def test_null_and_shape_errors(lib):
     # packed width must hold selections plus the count column
     assert lib.qsa_sparse_gqa(ctypes.byref(g), d, d, d, 1, d, 1, d, None, d, 4, None, 0,
                               None) == 2
-    # GQA group other than 8
+    # GQA groups: 1..8 and 16 run (a few rows split the selection over CTAs and
+    # need the workspace: refused without one); other groups are unsupported;
+    # Hq % Hkv != 0 is a shape error
     g2 = Q.make_gqa_cfg(16, 4, 64, 10)
     assert lib.qsa_sparse_gqa(ctypes.byref(g2), d, d, d, 1, d, 68, d, None, d, 4, None, 0,
+                              None) == 5
+    g12 = Q.make_gqa_cfg(48, 4, 64, 10)
+    assert lib.qsa_sparse_gqa(ctypes.byref(g12), d, d, d, 1, d, 68, d, None, d, 4, None, 0,
                               None) == 4
+    g_odd = Q.make_gqa_cfg(30, 4, 64, 10)
+    assert lib.qsa_sparse_gqa(ctypes.byref(g_odd), d, d, d, 1, d, 68, d, None, d, 4, None, 0,
+                              None) == 2
+    # the no-workspace entry point makes the same configuration checks
+    assert lib.qsa_sparse_gqa_noalloc(ctypes.byref(g12), d, d, d, 1, d, 68, d, None, d, 4,
+                                      None) == 4
+    assert lib.qsa_sparse_gqa_noalloc(ctypes.byref(g_odd), d, d, d, 1, d, 68, d, None, d, 4,
+                                      None) == 2
     # page size not a multiple of 16
     g3 = Q.make_gqa_cfg(32, 4, 40, 10)
     assert lib.qsa_sparse_gqa(ctypes.byref(g3), d, d, d, 1, d, 68, d, None, d, 4, None, 0,

@@ -55,6 +55,15 @@ MID = {
                                            contexts=(1500, 2603), rows_per_req=(70, 66),
                                            n_heads=8, index_dtype=E4, compress_ratio=4,
                                            token_topk=256, hq=8, hkv=1, page=32),
+    # query-head groups other than 8 (the pages only need Hq % Hkv == 0)
+    "mid_group16": W.small_spec("mid_group16", seed=19, contexts=(3000, 900, 4100),
+                                rows_per_req=(2, 1, 3), n_heads=16, index_dtype=E4,
+                                compress_ratio=4, token_topk=512, hq=32, hkv=2, page=64),
+    "mid_group4": W.small_spec("mid_group4", seed=20, contexts=(2500, 77, 3333),
+                               rows_per_req=(3, 1, 2), n_heads=8, index_dtype=BF,
+                               compress_ratio=4, token_topk=256, hq=16, hkv=4, page=32),
+    "small_group3": W.small_spec("small_group3", seed=22, hq=6, hkv=2),
+    "small_group1": W.small_spec("small_group1", seed=23, hq=4, hkv=4),
 }
 
 
@@ -179,7 +188,8 @@ def test_topk_matches_oracle(ratio, topk, positions, ties):
 
 # ----------------------------------------------------------------- stage 4
 @pytest.mark.parametrize("name", ["tiny_bf16", "small_bf16_copy_path", "mid_e4m3_r4",
-                                  "mid_h64_e4m3_r2", "mid_mrope_h8"])
+                                  "mid_h64_e4m3_r2", "mid_mrope_h8", "mid_group16", "mid_group4",
+                                  "small_group3", "small_group1"])
 @pytest.mark.parametrize("gate", [True, False])
 def test_sparse_gqa_matches_oracle(name, gate):
     spec = MID[name]
@@ -205,6 +215,40 @@ def test_sparse_gqa_matches_oracle(name, gate):
         ok, err = close_bf16(got[row], want)
         assert ok, f"row {row} (n={n}): max err {err:.3g}"
     assert (got[-1] == 0).all()
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 4), (32, 2)])
+def test_sparse_gqa_many_rows_ragged(hq, hkv):
+    """Many (row, KV head) pairs (the prefill shape: several waves of CTAs,
+    no split-KV), with ragged selections: counts from 0 to the full width,
+    and rows whose selection is the whole prefix."""
+    rows = 1400
+    rng = np.random.default_rng(hq + hkv)
+    contexts = [int(x) for x in rng.integers(5, 400, size=rows)]
+    spec = W.small_spec("many_pairs", seed=24 + hkv, contexts=contexts, rows_per_req=[1] * rows,
+                        n_heads=8, index_dtype=BF, compress_ratio=4, token_topk=64, hq=hq,
+                        hkv=hkv, page=16)
+    wl = W.make_workload(spec, device="cuda")
+    _, gcfg = cfgs(spec, wl)
+    assert Q.gqa_splits(gcfg, spec.rows, spec.packed_width) == 1
+    st = OracleState(wl, with_kv=False)
+    packed_np = random_packed(rng, st.cfg, st.logical_positions, full_rows=set(range(0, rows, 7)))
+    packed_np[5, :] = -1
+    packed_np[5, -1] = 0
+    out = torch.full_like(wl["q"], 3.0)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], torch.from_numpy(packed_np).cuda(),
+                 wl["token_to_req"], wl["gate"], out, ws)
+    torch.cuda.synchronize()
+    got = f64(out)
+    for row in list(range(0, rows, 13)) + [5, rows - 1]:
+        n = int(packed_np[row, -1])
+        req = int(st.token_to_req[row])
+        want = oracle_gqa_row(st.q[row], wl["kv"], st.block_table[req], packed_np[row, :n],
+                              spec.page, st.gate[row])
+        ok, err = close_bf16(got[row], want)
+        assert ok, f"row {row} (n={n}): max err {err:.3g}"
+    assert (got[5] == 0).all()
 
 
 def test_split_kv_invariance():
