@@ -48,6 +48,11 @@ R11 1-D RoPE (all sections 0): the query uses positions[row, 0, 0]; a
 R12 e4m3: round to nearest even, saturate to +-448 (OCP FP8 E4M3FN), never
     NaN.  bf16: round to nearest even.
 R13 gate: out = bf16(bf16(attn) * sigmoid(gate)); no gate: bf16(attn).
+R15 FP8 main KV cache: stored value e4m3(x / scale) with a static scalar
+    scale per tensor (k_scale for K, v_scale for V); attention reads the
+    stored values unscaled, multiplies each score by k_scale (with
+    head_dim^-0.5) and the normalised output by v_scale before its bf16
+    rounding.
 R14 the pooled group of a row is the ratio tokens ending at its logical
     position p; members at or after the first logical position of the
     request's rows in this step are read from this step's raw keys, older
@@ -124,6 +129,15 @@ def e4m3_decode_table() -> np.ndarray:
 
 def e4m3_decode(codes) -> np.ndarray:
     return e4m3_decode_table()[np.asarray(codes, dtype=np.uint8)]
+
+
+def quantize_kv_e4m3(x, scale: float) -> np.ndarray:
+    """FP8 KV-cache write with a static per-tensor scale: the stored value is
+    e4m3(x / scale), saturated to +-448 ("vllm.models.qwen4_exp.nvidia.qsa",
+    Qwen4ExpQSABackend: e4m3 bytes written by reshape_and_cache with the
+    layer's per-tensor scales; the patch notes the writer clamps to +-448).
+    Returns the stored (unscaled) values."""
+    return round_e4m3(np.asarray(x, dtype=np.float64) / float(scale))
 
 
 def e4m3_encode(x) -> np.ndarray:
@@ -437,7 +451,8 @@ def sigmoid(x):
     return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
 
 
-def sparse_gqa_row(q_row, kv, block_row, tokens, page: int, gate_row=None) -> np.ndarray:
+def sparse_gqa_row(q_row, kv, block_row, tokens, page: int, gate_row=None,
+                   k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
     """Sparse GQA for one row over its selected tokens.
 
     Follows "0002-qwen4_exp-FP8-E4M3-KV-reader-for-QSA..." patch,
@@ -447,8 +462,14 @@ def sparse_gqa_row(q_row, kv, block_row, tokens, page: int, gate_row=None) -> np
     the gate) and "vllm.models.qwen4_exp.nvidia.qsa", Qwen4ExpQSAImpl.forward
     (K and V are the two halves of the last axis of the paged cache).
 
-    q_row: [Hq, D]; kv: [blocks, Hkv, page, 2D]; tokens: request-relative
-    token indices; gate_row: [Hq, D] or None.  Returns bf16 values [Hq, D].
+    FP8 cache (the same patch, KV_DTYPE branches): K and V hold the decoded
+    e4m3 values as stored (unscaled); the static scalar k_scale multiplies
+    every score (together with head_dim^-0.5) and v_scale the normalised
+    attention output, before its bf16 rounding.  A bf16 cache uses 1 for both.
+
+    q_row: [Hq, D]; kv: [blocks, Hkv, page, 2D] (values); tokens:
+    request-relative token indices; gate_row: [Hq, D] or None.  Returns bf16
+    values [Hq, D].
     """
     q_row = np.asarray(q_row, dtype=np.float64)
     Hq, D = q_row.shape
@@ -464,9 +485,9 @@ def sparse_gqa_row(q_row, kv, block_row, tokens, page: int, gate_row=None) -> np
             rows = np.asarray(kv[blocks, kvh, offs], dtype=np.float64)  # [n, 2D]
             k = rows[:, :D]
             v = rows[:, D:]
-            z = k @ q_row[hq] / math.sqrt(D)
+            z = (k @ q_row[hq]) * (float(k_scale) / math.sqrt(D))
             w = np.exp(z - z.max())
-            attn[hq] = (w / w.sum()) @ v
+            attn[hq] = ((w / w.sum()) @ v) * float(v_scale)
     out = round_bf16(attn)
     if gate_row is not None:
         out = round_bf16(out * sigmoid(gate_row))
@@ -481,7 +502,8 @@ def layer_step(cfg: QsaConfig, *, projected_q, raw_keys, positions, cos_sin,
                q_norm_w, k_norm_w, ring, ring_pos, ring_block_table,
                token_to_req, query_start_loc, logical_positions, ccache,
                compressed_slots, cblock_table, q, kv, block_table, page,
-               gate=None, packed=None, skip_topk=False, rows_to_score=None):
+               gate=None, packed=None, skip_topk=False, rows_to_score=None,
+               k_scale=1.0, v_scale=1.0):
     """O1..O7 in order: stage 1 on every row, then (unless skip_topk) stages
     2-3, then stage 4.  With skip_topk the given ``packed`` buffer (from the
     step that selected) feeds stage 4 unchanged (QSAIndexer.skip_topk:
@@ -516,5 +538,5 @@ def layer_step(cfg: QsaConfig, *, projected_q, raw_keys, positions, cos_sin,
         req = int(token_to_req[row])
         n = int(packed[row, -1])
         out[row] = sparse_gqa_row(q[row], kv, block_table[req], packed[row, :n], page,
-                                  None if gate is None else gate[row])
+                                  None if gate is None else gate[row], k_scale, v_scale)
     return q_idx, packed, out

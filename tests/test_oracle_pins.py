@@ -540,3 +540,56 @@ def test_prep_query_hand_worked_two_heads_mrope():
     swapped = O.gemma_rmsnorm(O.rope_neox(x.reshape(2, 128), (T, H, Wd), cs, 64, (8, 12, 12)),
                               w, 0.0)
     assert np.abs(O.round_bf16(swapped) - got).max() > 0.1
+
+
+# --------------------------------------------------------------------------
+# FP8 main KV cache (static scalar scales)
+# --------------------------------------------------------------------------
+
+def test_fp8_kv_write_matches_torch_e4m3_of_scaled_values():
+    """Reading R15, the cache write: e4m3(x / scale), saturating at +-448."""
+    x = RNG.standard_normal(20000).astype(np.float32).astype(np.float64)
+    for scale in (1.0, 0.0625, 0.013):
+        want = torch.from_numpy((x / scale).astype(np.float32)).to(torch.float8_e4m3fn)
+        want = want.to(torch.float64).numpy()
+        fin = np.abs(x / scale) < 440  # torch's cast is not defined to saturate
+        np.testing.assert_array_equal(O.quantize_kv_e4m3(x, scale)[fin], want[fin])
+    np.testing.assert_array_equal(O.quantize_kv_e4m3([1e5, -1e5], 1.0), [448.0, -448.0])
+
+
+def _fp8_case(L=180, Hq=8, Hkv=2, page=16, D=128):
+    nb = -(-L // page) + 2
+    kv = O.round_e4m3(RNG.standard_normal((nb, Hkv, page, 2 * D)) * 20.0)  # stored values
+    bt = RNG.permutation(nb)[: -(-L // page)]
+    q = O.round_bf16(RNG.standard_normal((Hq, D)))
+    return kv, bt, q
+
+
+def test_fp8_kv_scales_fold_into_scores_and_output():
+    """A k_scale applied to the scores equals the keys scaled by it, and a
+    v_scale applied to the output equals the values scaled by it (the patch's
+    "scaling each score is equivalent to scaling every key element" and "the
+    attention output is linear in V")."""
+    kv, bt, q = _fp8_case()
+    toks = RNG.choice(180, size=70, replace=False)
+    ks, vs = 0.0173, 0.049
+    got = O.sparse_gqa_row(q, kv, bt, toks, 16, k_scale=ks, v_scale=vs)
+    scaled = kv.copy()
+    scaled[..., :128] *= ks
+    scaled[..., 128:] *= vs
+    want = O.sparse_gqa_row(q, scaled, bt, toks, 16)
+    # both are bf16 roundings of the same fp64 quantity up to ~1e-15
+    assert np.abs(got - want).max() <= np.abs(want).max() * 2.0 ** -7
+    assert (got == want).mean() > 0.99
+
+
+def test_fp8_kv_all_selected_equals_dense_sdpa_on_dequantized_cache():
+    kv, bt, q = _fp8_case(L=150)
+    ks, vs = 0.05, 0.031
+    toks = np.arange(150)
+    got = O.sparse_gqa_row(q, kv, bt, toks, 16, k_scale=ks, v_scale=vs)
+    rows = kv[bt[toks // 16], :, toks % 16]  # [L, Hkv, 2D]
+    k = torch.from_numpy(rows[..., :128] * ks).permute(1, 0, 2).repeat_interleave(4, 0)
+    v = torch.from_numpy(rows[..., 128:] * vs).permute(1, 0, 2).repeat_interleave(4, 0)
+    ref = F.scaled_dot_product_attention(torch.from_numpy(q)[:, None, :], k, v)[:, 0].numpy()
+    np.testing.assert_array_equal(got, O.round_bf16(ref))
