@@ -95,7 +95,8 @@ def config_of(spec, world: int) -> dict:
             "contexts": f"{min(spec.contexts)}..{max(spec.contexts)}",
             "indexer": f"{spec.n_heads}x128 {'e4m3' if spec.index_dtype else 'bf16'}"
                        f" r={spec.compress_ratio} topk={spec.token_topk}",
-            "gqa": f"{spec.hq}q/{spec.hkv}kv x128 bf16 page {spec.page}",
+            "gqa": f"{spec.hq}q/{spec.hkv}kv x128 "
+                   f"{'e4m3 (static scales)' if spec.kv_dtype else 'bf16'} page {spec.page}",
             "parallelism": f"replicas x{world}",
             "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, then a "
                   f"{DRAIN_BYTES >> 20} MiB read to evict the written lines)"}
@@ -280,7 +281,9 @@ def build(spec, device):
     cfg = Q.make_cfg(spec.n_heads, spec.compress_ratio, spec.token_topk, spec.index_dtype,
                      spec.cpage, wl["cos_sin"].shape[0], state_size=spec.S,
                      mrope_section=spec.mrope_section, eps=spec.eps)
-    gcfg = Q.make_gqa_cfg(spec.hq, spec.hkv, spec.page, wl["kv"].shape[0])
+    ks = spec.kv_scale if spec.kv_dtype == W.DTYPE_E4M3 else 1.0
+    gcfg = Q.make_gqa_cfg(spec.hq, spec.hkv, spec.page, wl["kv"].shape[0], kv_dtype=spec.kv_dtype,
+                          k_scale=ks, v_scale=ks)
     mv = max(spec.contexts) // spec.compress_ratio
     packed = torch.empty((spec.rows, spec.packed_width), dtype=torch.int32, device=device)
     out = torch.empty_like(wl["q"])
@@ -296,6 +299,7 @@ def algorithmic_bytes(spec, wl, packed):
     logical = wl["logical_positions"].cpu().numpy().astype(np.int64)
     qsl = wl["query_start_loc"].cpu().numpy()
     e_idx = 1 if spec.index_dtype == W.DTYPE_E4M3 else 2
+    e_kv = 1 if spec.kv_dtype == W.DTYPE_E4M3 else 2
     D, r = 128, spec.compress_ratio
     pk = packed.cpu().numpy()
     keys = kv = 0
@@ -307,7 +311,7 @@ def algorithmic_bytes(spec, wl, packed):
         union = set()
         for row in range(a, b):
             union.update(pk[row, :counts[row]].tolist())
-        kv += len(union) * spec.hkv * 2 * D * 2
+        kv += len(union) * spec.hkv * 2 * D * e_kv
     rows = spec.rows
     groups = int((wl["compressed_slots"] >= 0).sum().item())
     stage1 = rows * (spec.n_heads * D * 2 + 2 * D * 2 + spec.n_heads * D * e_idx) + groups * (
@@ -315,7 +319,7 @@ def algorithmic_bytes(spec, wl, packed):
     main_io = rows * 3 * spec.hq * D * 2
     packed_io = rows * 2 * 4 * spec.packed_width
     step = keys + kv + stage1 + main_io + packed_io
-    gqa = int(counts.sum()) * spec.hkv * 2 * D * 2 + main_io + rows * 4 * spec.packed_width
+    gqa = int(counts.sum()) * spec.hkv * 2 * D * e_kv + main_io + rows * 4 * spec.packed_width
     return step, gqa, {"compressed_keys": keys, "kv_gather": kv, "stage1": stage1,
                        "main_qkv_gate_out": main_io, "packed": packed_io}
 
@@ -688,6 +692,8 @@ def run_ours(args):
                  "prefill": prefill_report(device, 3, flush, drain, fp8, bf16,
                                            not args.no_cpu_baseline),
                  "long_decode": decode_report("long_decode", device, 10, 3, flush, drain, hbm),
+                 "decode_batch_fp8kv": decode_report("decode_batch_fp8kv", device, 10, 3, flush,
+                                                     drain, hbm),
                  "mtp_mrope": mtp_report(device, 10, 3, flush, drain, hbm)}
 
     if rank == 0:

@@ -91,6 +91,14 @@ typedef struct qsa_gqa_cfg {
   int32_t head_dim;      /* must be 128 */
   int32_t page_size;     /* tokens per KV block, a multiple of 16 */
   int32_t num_blocks;    /* KV blocks in the cache */
+  /* KV cache element type ("0002-qwen4_exp-FP8-E4M3-KV-reader-for-QSA..."
+   * patch; Qwen4ExpQSABackend.supported_kv_cache_dtypes "fp8_e4m3"):
+   * QSA_DTYPE_BF16 (0, scales unused) or QSA_DTYPE_E4M3 (1): the cache holds
+   * e4m3(x / scale) per tensor, and the reader folds k_scale into the scores
+   * and v_scale into the normalised output.  e4m3 needs finite scales > 0. */
+  int32_t kv_dtype;
+  float k_scale;
+  float v_scale;
 } qsa_gqa_cfg;
 
 /*
@@ -188,7 +196,8 @@ qsa_status qsa_topk(const qsa_cfg* cfg, const float* logits, int64_t ld,
  * n == 0, split-KV partials in fp32 merged by log-sum-exp, then
  * out = bf16(bf16(attn) * sigmoid(gate)) (or bf16(attn) when gate is NULL).
  *  q      [rows, Hq, D] bf16
- *  kv     [num_blocks, Hkv, page_size, 2*D] bf16 (K in [..., :D], V in [..., D:])
+ *  kv     [num_blocks, Hkv, page_size, 2*D] in the cfg's kv_dtype (bf16, or e4m3
+ *         bytes), K in [..., :D], V in [..., D:]
  *  block_table [reqs, bt_stride] int32: token t of request q is in block
  *         block_table[q, t / page_size], offset t % page_size
  *  packed [rows, packed_width] int32; token_to_req [rows]
@@ -260,7 +269,7 @@ typedef struct qsa_step_args {
   const int32_t* logical_positions; /* [rows] */
   int32_t* packed;                  /* [rows, token_topk + r] (out, or in with skip_topk) */
   const void* q;                    /* [rows, Hq, D] bf16 */
-  const void* kv;                   /* [num_blocks, Hkv, page, 2D] bf16 */
+  const void* kv;                   /* [num_blocks, Hkv, page, 2D] bf16 or e4m3 */
   const int32_t* block_table;       /* [reqs, bt_stride] */
   int32_t bt_stride;
   const void* gate;                 /* [rows, Hq, D] bf16 or NULL */

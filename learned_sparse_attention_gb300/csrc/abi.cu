@@ -378,7 +378,10 @@ qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
   if (a16 & 15) return QSA_ERR_INVALID_ARG;
   GqaParams p{};
   p.q = static_cast<const uint16_t*>(q);
-  p.kv = static_cast<const uint16_t*>(kv);
+  p.kv = kv;
+  p.kv_dtype = gcfg->kv_dtype;
+  p.k_scale = gcfg->k_scale;
+  p.v_scale = gcfg->v_scale;
   p.block_table = block_table;
   p.packed = packed;
   p.token_to_req = token_to_req;
@@ -464,6 +467,10 @@ qsa_status check_gcfg(const qsa_gqa_cfg* g) {
   if (group > 8 && group != 16) return QSA_ERR_UNSUPPORTED;
   if (g->page_size < 16 || g->page_size % 16 != 0) return QSA_ERR_SHAPE;
   if (g->num_blocks < 1) return QSA_ERR_SHAPE;
+  if (g->kv_dtype != QSA_DTYPE_BF16 && g->kv_dtype != QSA_DTYPE_E4M3) return QSA_ERR_DTYPE;
+  if (g->kv_dtype == QSA_DTYPE_E4M3 &&
+      !(g->k_scale > 0.f && g->v_scale > 0.f && g->k_scale < 3.0e38f && g->v_scale < 3.0e38f))
+    return QSA_ERR_INVALID_ARG;
   return QSA_OK;
 }
 

@@ -88,7 +88,7 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl);
 
 struct GqaParams {
   const uint16_t* q;       // [rows, Hq, 128]
-  const uint16_t* kv;      // [blocks, Hkv, page, 256]
+  const void* kv;          // [blocks, Hkv, page, 256] bf16 or e4m3 (kv_dtype)
   const int32_t* block_table;
   const int32_t* packed;
   const int32_t* token_to_req;
@@ -99,6 +99,8 @@ struct GqaParams {
   unsigned* counters;      // [rows, Hkv] merge tickets, or null for a separate merge launch
   int bt_stride, packed_width;
   int rows, hq, hkv, group, page, num_blocks, splits;  // group = hq / hkv: 1..8 or 16
+  int kv_dtype;            // 0: bf16, 1: e4m3 with static scales
+  float k_scale, v_scale;  // e4m3: stored value * scale = cached value
   unsigned long long* err;
 };
 // Split-KV factor for `rows` rows on a device with `sms` multiprocessors.

@@ -45,13 +45,23 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kRidBatch = 8;  // KV row ids resolved per thread per batch
 constexpr int kFirst = 20;    // packed entries per thread loaded right after the wait
 constexpr int kTile = 64;      // tokens per CTA tile (16 per warp)
-constexpr int kStages = 3;
-constexpr int kSlab = 16 * 512;  // bytes per warp stage: 16 tokens x (K|V)
-constexpr int kPipe = kWarps * kStages * kSlab;
 constexpr int kMaxTiles = 40;                // tiles of one row-id chunk
 constexpr int kMaxTok = kMaxTiles * kTile;   // token row ids staged at a time
-constexpr int kSmem = kPipe + kMaxTok * 4;
 constexpr uint32_t kBadRow = 0xFFFFFFFFu;
+
+// Shared-memory plan per KV dtype (KVT 0: bf16, 1: e4m3).  A warp's stage
+// holds its 16 tokens' K rows, then their V rows, in 16-byte chunks
+// XOR-swizzled by token.  e4m3 rows are half as wide, so the ring is deeper
+// at the same footprint, and each warp has an f16 tile it decodes V into.
+template <int KVT>
+struct KvPlan {
+  static constexpr int kRowB = KVT ? 256 : 512;          // K|V bytes of one (token, KV head)
+  static constexpr int kStages = KVT ? 5 : 3;
+  static constexpr int kSlab = 16 * kRowB;                // bytes per warp stage
+  static constexpr int kPipe = kWarps * kStages * kSlab;
+  static constexpr int kVf16 = KVT ? kWarps * 16 * 256 : 0;  // per-warp f16 V tiles
+  static constexpr int kSmem = kPipe + kVf16 + kMaxTok * 4;
+};
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
@@ -112,12 +122,18 @@ __device__ __forceinline__ uint32_t kv_row_id(const GqaParams& P, int off, int p
 }
 
 // NB: column blocks of 8 query heads (1 for groups of 1-8, 2 for 16).
-template <int NB>
+// KVT: KV cache dtype, 0 bf16, 1 e4m3 with static scales (f16 MMAs: every
+// e4m3 value and every bf16 query of normal range is exact in f16).
+template <int NB, int KVT>
 __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
+  using KP = KvPlan<KVT>;
+  constexpr int kStages = KP::kStages;
+  constexpr int kSlab = KP::kSlab;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_vmask[kWarps][kStages];
   __shared__ int s_last;
-  uint32_t* s_rowid = reinterpret_cast<uint32_t*>(smem + kPipe);
+  uint32_t* s_rowid = reinterpret_cast<uint32_t*>(smem + KP::kPipe + KP::kVf16);
+  const uint8_t* kvb = static_cast<const uint8_t*>(P.kv);
   // KV-head-major CTA order: the CTAs resident at one time mostly share a
   // KV head, so the rows of a request that select the same tokens (prefill
   // chunks, speculative rows) find them in L2
@@ -143,8 +159,17 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
     const uint16_t* qh = P.q + (static_cast<long long>(row) * P.hq + kvh * G + min(hl, G - 1)) * 128;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      qb[nb][kk][0] = hl < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t) : 0u;
-      qb[nb][kk][1] = hl < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t) : 0u;
+      if (KVT == 0) {
+        qb[nb][kk][0] = hl < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t) : 0u;
+        qb[nb][kk][1] = hl < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t) : 0u;
+      } else {
+        // f16 B fragments over the same dimension order as the decoded e4m3
+        // K fragments: k-step kk pairs (2t, 2t+1) <- dims 16 kk + 4t + {0, 1}
+        // and (2t+8, 2t+9) <- dims 16 kk + 4t + {2, 3}
+        const uint2 v = hl < G ? *reinterpret_cast<const uint2*>(qh + 16 * kk + 4 * t) : make_uint2(0u, 0u);
+        qb[nb][kk][0] = bf16x2_to_f16x2(v.x);
+        qb[nb][kk][1] = bf16x2_to_f16x2(v.y);
+      }
     }
   }
   // The request's block-table row (a caller input) is copied before the
@@ -155,6 +180,7 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   const int32_t* bt_row = P.block_table + static_cast<long long>(req < 0 ? 0 : req) * P.bt_stride;
   int32_t* s_bt = reinterpret_cast<int32_t*>(smem + (kStages - 1) * kWarps * kSlab);
   const bool bt_fits = P.bt_stride <= kWarps * kSlab / 4;
+  const float vscale = KVT ? P.v_scale : 1.0f;
   if (bt_fits) {
     for (int i0 = threadIdx.x; i0 < P.bt_stride; i0 += 8 * kThreads) {
       int v[8];
@@ -214,7 +240,8 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
     m0[nb] = m1[nb] = -INFINITY;
     l0[nb] = l1[nb] = 0.f;
   }
-  const float sl2 = 0.08838834764831845f * kLog2e;  // 128^-0.5 * log2(e)
+  // 128^-0.5 * log2(e), and the static K scale of an e4m3 cache folded in
+  const float sl2 = 0.08838834764831845f * kLog2e * (KVT ? P.k_scale : 1.0f);
   bool bad = false;
 
   // KV row ids of the selected tokens tok[u] (u < NB) into
@@ -279,14 +306,27 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
       const uint32_t vm = __ballot_sync(0xffffffffu, rid != kBadRow) & 0xffffu;
       if (lane == 0) s_vmask[warp][stage] = vm;
       uint8_t* dst_base = smem + (stage * kWarps + warp) * kSlab;
-      const int chunk = lane & 15, is_v = lane >> 4;
+      if (KVT == 0) {  // one 512-byte row per instruction
+        const int chunk = lane & 15, is_v = lane >> 4;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
-        const bool okj = (vm >> j) & 1u;
-        uint8_t* dst = dst_base + is_v * 4096 + j * 256 + ((chunk ^ (j & 7)) << 4);
-        const uint16_t* src = P.kv + static_cast<long long>(okj ? rj : 0u) * 256 + is_v * 128 + chunk * 8;
-        cp_async16(dst, src, okj ? 16u : 0u);
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
+          const bool okj = (vm >> j) & 1u;
+          uint8_t* dst = dst_base + is_v * 4096 + j * 256 + ((chunk ^ (j & 7)) << 4);
+          const uint8_t* src = kvb + static_cast<long long>(okj ? rj : 0u) * 512 + is_v * 256 + chunk * 16;
+          cp_async16(dst, src, okj ? 16u : 0u);
+        }
+      } else {  // two 256-byte rows per instruction
+        const int chunk = lane & 7, is_v = (lane >> 3) & 1, sub = lane >> 4;
+#pragma unroll
+        for (int j2 = 0; j2 < 8; ++j2) {
+          const int j = 2 * j2 + sub;
+          const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
+          const bool okj = (vm >> j) & 1u;
+          uint8_t* dst = dst_base + is_v * 2048 + j * 128 + ((chunk ^ (j & 7)) << 4);
+          const uint8_t* src = kvb + static_cast<long long>(okj ? rj : 0u) * 256 + is_v * 128 + chunk * 16;
+          cp_async16(dst, src, okj ? 16u : 0u);
+        }
       }
     };
 
@@ -300,7 +340,7 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
       __syncwarp();
       const int stage = it % kStages;
       const uint8_t* sK = smem + (stage * kWarps + warp) * kSlab;
-      const uint8_t* sV = sK + 4096;
+      const uint8_t* sV = sK + 8 * KP::kRowB;
       // S^T = K.Q^T over 8 K-steps, split over four accumulators so that the
       // MMAs form four dependent chains of two instead of one of eight (each
       // K fragment feeds every column block)
@@ -309,14 +349,36 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
       for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
         for (int c = 0; c < 4; ++c) sa[nb][c][0] = sa[nb][c][1] = sa[nb][c][2] = sa[nb][c][3] = 0.f;
+      if (KVT == 0) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t a[4];
-        const int rl = lane & 15;
-        const int ch = 2 * kk + (lane >> 4);
-        ldmatrix_x4(a, sK + rl * 256 + ((ch ^ (rl & 7)) << 4));
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t a[4];
+          const int rl = lane & 15;
+          const int ch = 2 * kk + (lane >> 4);
+          ldmatrix_x4(a, sK + rl * 256 + ((ch ^ (rl & 7)) << 4));
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sa[nb][kk & 3], a, qb[nb][kk][0], qb[nb][kk][1]);
+          for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sa[nb][kk & 3], a, qb[nb][kk][0], qb[nb][kk][1]);
+        }
+      } else {
+        // one ldmatrix.x4 brings 32 e4m3 dims of the warp's 16 rows: per lane
+        // dims 4t..4t+3 of rows g and g+8 for two 16-dim k-steps, decoded to
+        // the f16 A fragments in the order the query fragments use
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          uint32_t a[4];
+          const int rl = lane & 15;
+          const int ch = 2 * k2 + (lane >> 4);
+          ldmatrix_x4(a, sK + rl * 128 + ((ch ^ (rl & 7)) << 4));
+          const uint32_t fa[4] = {e4m3x2_to_f16x2(a[0] & 0xFFFFu), e4m3x2_to_f16x2(a[1] & 0xFFFFu),
+                                  e4m3x2_to_f16x2(a[0] >> 16), e4m3x2_to_f16x2(a[1] >> 16)};
+          const uint32_t fb[4] = {e4m3x2_to_f16x2(a[2] & 0xFFFFu), e4m3x2_to_f16x2(a[3] & 0xFFFFu),
+                                  e4m3x2_to_f16x2(a[2] >> 16), e4m3x2_to_f16x2(a[3] >> 16)};
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            mma_f16_16816(sa[nb][(2 * k2) & 3], fa, qb[nb][2 * k2][0], qb[nb][2 * k2][1]);
+            mma_f16_16816(sa[nb][(2 * k2 + 1) & 3], fb, qb[nb][2 * k2 + 1][0], qb[nb][2 * k2 + 1][1]);
+          }
+        }
       }
       const uint32_t vm = s_vmask[warp][stage];
       const bool v0 = (vm >> g) & 1u, v1 = (vm >> (g + 8)) & 1u;
@@ -360,17 +422,45 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
         l1[nb] += p1 + p3;
         m0[nb] = mn0;
         m1[nb] = mn1;
-        pb[nb][0] = movmatrix_trans(pack_bf16x2(p0, p1));
-        pb[nb][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+        pb[nb][0] = movmatrix_trans(KVT ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+        pb[nb][1] = movmatrix_trans(KVT ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
+      }
+      const uint8_t* sVt = sV;  // the V rows the transposed loads read (bf16 or f16)
+      if (KVT == 1) {
+        // decode the warp's 16 e4m3 V rows into its f16 tile (same swizzled
+        // layout as a bf16 V block): lane = row (lane & 15), half (lane >> 4)
+        uint8_t* vf = smem + KP::kPipe + warp * 4096;
+        const int j = lane & 15, hf = lane >> 4;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int c = 4 * hf + c4;
+          const uint4 raw = *reinterpret_cast<const uint4*>(sV + j * 128 + ((c ^ (j & 7)) << 4));
+          uint4 f0, f1;
+          f0.x = e4m3x2_to_f16x2(raw.x & 0xFFFFu);
+          f0.y = e4m3x2_to_f16x2(raw.x >> 16);
+          f0.z = e4m3x2_to_f16x2(raw.y & 0xFFFFu);
+          f0.w = e4m3x2_to_f16x2(raw.y >> 16);
+          f1.x = e4m3x2_to_f16x2(raw.z & 0xFFFFu);
+          f1.y = e4m3x2_to_f16x2(raw.z >> 16);
+          f1.z = e4m3x2_to_f16x2(raw.w & 0xFFFFu);
+          f1.w = e4m3x2_to_f16x2(raw.w >> 16);
+          *reinterpret_cast<uint4*>(vf + j * 256 + (((2 * c) ^ (j & 7)) << 4)) = f0;
+          *reinterpret_cast<uint4*>(vf + j * 256 + (((2 * c + 1) ^ (j & 7)) << 4)) = f1;
+        }
+        __syncwarp();
+        sVt = vf;
       }
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t a[4];
         const int tk = (lane & 7) + ((lane >> 4) << 3);
         const int ch = 2 * mt + ((lane >> 3) & 1);
-        ldmatrix_x4_trans(a, sV + tk * 256 + ((ch ^ (tk & 7)) << 4));
+        ldmatrix_x4_trans(a, sVt + tk * 256 + ((ch ^ (tk & 7)) << 4));
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[nb][mt], a, pb[nb][0], pb[nb][1]);
+        for (int nb = 0; nb < NB; ++nb) {
+          if (KVT == 0) mma_bf16_16816(o[nb][mt], a, pb[nb][0], pb[nb][1]);
+          else mma_f16_16816(o[nb][mt], a, pb[nb][0], pb[nb][1]);
+        }
       }
       __syncwarp();
       const int nxt = it + kStages - 1;
@@ -427,7 +517,9 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] += co[(w * 8 * NB + hh) * 128 + d0 + e] * wt;
     }
-    const float inv = L > 0.f ? 1.0f / L : 0.f;
+    // the static V scale of an e4m3 cache multiplies the normalised output
+    // (and every split partial alike: the merge is linear in them)
+    const float inv = L > 0.f ? vscale / L : 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] *= inv;
     const int hq = kvh * G + hh;
@@ -499,17 +591,22 @@ cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
   if (static_cast<long long>(p.num_blocks) * p.hkv * p.page >= static_cast<long long>(kBadRow))
     return cudaErrorInvalidValue;
   if (p.group < 1 || (p.group > 8 && p.group != 16)) return cudaErrorInvalidValue;
-  auto kern = p.group <= 8 ? gqa_kernel<1> : gqa_kernel<2>;
+  if (p.kv_dtype != 0 && p.kv_dtype != 1) return cudaErrorInvalidValue;
+  void (*kerns[2][2])(const GqaParams) = {{gqa_kernel<1, 0>, gqa_kernel<1, 1>},
+                                          {gqa_kernel<2, 0>, gqa_kernel<2, 1>}};
+  const int smems[2] = {KvPlan<0>::kSmem, KvPlan<1>::kSmem};
   const int ki = p.group <= 8 ? 0 : 1;
-  static bool attr_set[2][64] = {};
+  auto kern = kerns[ki][p.kv_dtype];
+  const int kSmem = smems[p.kv_dtype];
+  static bool attr_set[2][2][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[ki][dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[ki][p.kv_dtype][dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[ki][dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[ki][p.kv_dtype][dev] = true;
   }
   if (p.splits > 1 && p.counters != nullptr && zero_tickets) {
     cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(unsigned) * p.rows * p.hkv, stream);

@@ -81,7 +81,10 @@ extern "C" qsa_status qsa_sparse_gqa_noalloc(const qsa_gqa_cfg* gcfg, const void
 
   qsa::GqaParams p{};
   p.q = static_cast<const uint16_t*>(q);
-  p.kv = static_cast<const uint16_t*>(kv);
+  p.kv = kv;
+  p.kv_dtype = gcfg->kv_dtype;
+  p.k_scale = gcfg->k_scale;
+  p.v_scale = gcfg->v_scale;
   p.block_table = block_table;
   p.packed = packed;
   p.token_to_req = token_to_req;

@@ -41,7 +41,8 @@ class QsaCfg(ctypes.Structure):
 
 class QsaGqaCfg(ctypes.Structure):
     _fields_ = [("num_q_heads", _c_int), ("num_kv_heads", _c_int), ("head_dim", _c_int),
-                ("page_size", _c_int), ("num_blocks", _c_int)]
+                ("page_size", _c_int), ("num_blocks", _c_int), ("kv_dtype", _c_int),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class QsaStepArgs(ctypes.Structure):
@@ -117,10 +118,12 @@ def make_cfg(n_heads, compress_ratio, token_topk, index_dtype, cpage, max_positi
     return c
 
 
-def make_gqa_cfg(num_q_heads, num_kv_heads, page_size, num_blocks, head_dim=128) -> QsaGqaCfg:
+def make_gqa_cfg(num_q_heads, num_kv_heads, page_size, num_blocks, head_dim=128,
+                 kv_dtype=DTYPE_BF16, k_scale=1.0, v_scale=1.0) -> QsaGqaCfg:
     g = QsaGqaCfg()
     g.num_q_heads, g.num_kv_heads, g.head_dim = num_q_heads, num_kv_heads, head_dim
     g.page_size, g.num_blocks = page_size, num_blocks
+    g.kv_dtype, g.k_scale, g.v_scale = kv_dtype, k_scale, v_scale
     return g
 
 
@@ -186,7 +189,7 @@ def topk(cfg, logits, max_visible, logical_positions, packed, stream=None):
 
 def sparse_gqa(gcfg, q, kv, block_table, packed, token_to_req, gate, out, ws, stream=None):
     st = load().qsa_sparse_gqa(
-        ctypes.byref(gcfg), _ptr(q, torch.bfloat16), _ptr(kv, torch.bfloat16),
+        ctypes.byref(gcfg), _ptr(q, torch.bfloat16), _ptr(kv, _IDX),
         _ptr(block_table, torch.int32), block_table.shape[1], _ptr(packed, torch.int32),
         packed.shape[1], _ptr(token_to_req, torch.int32), _ptr(gate, torch.bfloat16),
         _ptr(out, torch.bfloat16), q.shape[0], _ptr(ws, torch.uint8),
@@ -205,7 +208,7 @@ def sparse_gqa_noalloc(gcfg, q, kv, block_table, packed, token_to_req, gate, out
     f = lib.qsa_sparse_gqa_noalloc
     f.argtypes = [_p, _p, _p, _p, _c_int, _p, _c_int, _p, _p, _p, _c_int, _p]
     f.restype = ctypes.c_int
-    st = f(ctypes.byref(gcfg), _ptr(q, torch.bfloat16), _ptr(kv, torch.bfloat16),
+    st = f(ctypes.byref(gcfg), _ptr(q, torch.bfloat16), _ptr(kv, _IDX),
            _ptr(block_table, torch.int32), block_table.shape[1], _ptr(packed, torch.int32),
            packed.shape[1], _ptr(token_to_req, torch.int32), _ptr(gate, torch.bfloat16),
            _ptr(out, torch.bfloat16), q.shape[0], _stream(stream))
@@ -245,7 +248,7 @@ def step_args(t: dict, packed, out, max_visible) -> QsaStepArgs:
     a.logical_positions = _ptr(t["logical_positions"], torch.int32)
     a.packed = _ptr(packed, torch.int32)
     a.q = _ptr(t["q"], torch.bfloat16)
-    a.kv = _ptr(t["kv"], torch.bfloat16)
+    a.kv = _ptr(t["kv"], _IDX)
     a.block_table = _ptr(t["block_table"], torch.int32)
     a.bt_stride = t["block_table"].shape[1]
     a.gate = _ptr(t.get("gate"), torch.bfloat16)

@@ -9,7 +9,9 @@ and the smoke check.
 Workload recipe (all values seeded):
 * activations (indexer projections, raw keys, main Q, gate) ~ N(0, 1), bf16;
 * RMSNorm weights ~ N(0, 0.1), bf16;
-* main paged K/V cache ~ N(0, 1), bf16, layout [blocks, Hkv, page, 2*D];
+* main paged K/V cache ~ N(0, 1), bf16, layout [blocks, Hkv, page, 2*D]; the
+  FP8 variant stores e4m3(x / kv_scale) of the same values (kv_scale = 1/16
+  for K and V: the stored values span about +-64, inside e4m3's +-448);
 * compressed-key cache ~ N(0, 1) rounded to the indexer dtype (e4m3 or
   bf16), layout [cpages, cpage, 1, D] with cpage = page / compress_ratio;
 * compressor-state ring ~ N(0, 1), bf16, layout [ring_blocks, S, 1, D]
@@ -61,6 +63,8 @@ class WorkloadSpec:
     image_span: int = 0       # MRoPE image-span length per request (0 = text only)
     mtp_steps: int = 1        # steps 1.. reuse step 0's selection (skip_topk)
     state_size: int = 0       # 0 -> 2 * compress_ratio
+    kv_dtype: int = DTYPE_BF16  # main KV cache: bf16, or e4m3 with a static scale
+    kv_scale: float = 1.0 / 16  # e4m3 cache: stored value = e4m3(x / kv_scale), K and V alike
 
     @property
     def cpage(self) -> int:
@@ -107,10 +111,13 @@ def named_spec(name: str) -> WorkloadSpec:
     if name == "mtp_mrope":
         return WorkloadSpec(name, 4, [65536] * 32, [4] * 32, index_dtype=DTYPE_BF16,
                             mrope_section=(8, 12, 12), image_span=1024, mtp_steps=4)
+    if name == "decode_batch_fp8kv":  # the decode batch over an FP8-e4m3 main KV cache
+        return WorkloadSpec(name, 1, _decode_contexts(1), [1] * 64, kv_dtype=DTYPE_E4M3)
     raise KeyError(name)
 
 
-NAMED = ("tiny_bf16", "decode_batch", "chunked_prefill", "long_decode", "mtp_mrope")
+NAMED = ("tiny_bf16", "decode_batch", "chunked_prefill", "long_decode", "mtp_mrope",
+         "decode_batch_fp8kv")
 
 
 def rope_cos_sin(max_pos: int, rotary_dim: int, theta: float = 10000.0) -> torch.Tensor:
@@ -284,6 +291,7 @@ def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0, with_caches: 
         t["ccache"] = cc.to(torch.bfloat16)
 
     if spec.peak_frac > 0 and with_kv:
+        assert spec.kv_dtype == DTYPE_BF16, "peaked positions are placed in a bf16 cache"
         for req in range(reqs):
             tok = peaks[req]
             L = spec.contexts[req]
@@ -302,6 +310,14 @@ def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0, with_caches: 
             for tt in range(max(0, firstpos - S), firstpos):
                 if tt in peaked:
                     t["ring"][rb, tt % S] *= 8
+    if spec.kv_dtype == DTYPE_E4M3:
+        # the same N(0, 1) values, stored as e4m3(x / kv_scale) (all inside +-448)
+        kv = t["kv"]
+        q8 = torch.empty(kv.shape, dtype=torch.uint8, device=kv.device)
+        for b0 in range(0, kv.shape[0], 4096):  # bounded temporaries
+            x = kv[b0:b0 + 4096].float() / spec.kv_scale
+            q8[b0:b0 + 4096] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        t["kv"] = q8
     t = {k: (v.to(dev) if v.device != dev else v) for k, v in t.items()}
     return Workload(spec, t, image_start)
 

@@ -17,8 +17,14 @@ def cfgs(spec, wl):
     cfg = Q.make_cfg(spec.n_heads, spec.compress_ratio, spec.token_topk, spec.index_dtype,
                      spec.cpage, wl["cos_sin"].shape[0], state_size=spec.S,
                      mrope_section=spec.mrope_section, eps=spec.eps)
-    gcfg = Q.make_gqa_cfg(spec.hq, spec.hkv, spec.page, wl["kv"].shape[0])
+    gcfg = Q.make_gqa_cfg(spec.hq, spec.hkv, spec.page, wl["kv"].shape[0], kv_dtype=spec.kv_dtype,
+                          k_scale=kv_scales(spec)[0], v_scale=kv_scales(spec)[1])
     return cfg, gcfg
+
+
+def kv_scales(spec):
+    """(k_scale, v_scale) of the workload's main KV cache (1, 1 for bf16)."""
+    return (spec.kv_scale, spec.kv_scale) if spec.kv_dtype == W.DTYPE_E4M3 else (1.0, 1.0)
 
 
 def max_visible(spec) -> int:
@@ -67,12 +73,13 @@ def gather_token_kv(kv: torch.Tensor, block_row, tokens, page: int) -> np.ndarra
     return f64(rows)[:, :, None, :]
 
 
-def oracle_gqa_row(q_row, kv: torch.Tensor, block_row, tokens, page, gate_row):
+def oracle_gqa_row(q_row, kv: torch.Tensor, block_row, tokens, page, gate_row, scales=(1.0, 1.0)):
     """Oracle stage 4 on one row, with the KV rows of its tokens gathered
     from the device cache and re-indexed as one-token pages."""
     compact = gather_token_kv(kv, block_row, tokens, page)
     n = len(tokens)
-    return O.sparse_gqa_row(q_row, compact, np.arange(n), np.arange(n), 1, gate_row)
+    return O.sparse_gqa_row(q_row, compact, np.arange(n), np.arange(n), 1, gate_row,
+                            k_scale=scales[0], v_scale=scales[1])
 
 
 def random_packed(rng, cfg: O.QsaConfig, logical, full_rows=()):

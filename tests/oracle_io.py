@@ -55,7 +55,9 @@ class OracleState:
         self.block_table = i64(t["block_table"])
         self.q = f64(t["q"])
         self.gate = f64(t["gate"])
-        self.kv = f64(t["kv"]) if with_kv else None
+        self.kv = f64(t["kv"]) if with_kv else None  # e4m3 caches: the stored values
+        self.kv_scales = ((s.kv_scale, s.kv_scale) if getattr(s, "kv_dtype", 0) == 1
+                          else (1.0, 1.0))
 
     def step(self, skip_topk=False, packed=None, rows_to_score=None, gate=True):
         return O.layer_step(
@@ -68,7 +70,7 @@ class OracleState:
             cblock_table=self.cblock_table, q=self.q, kv=self.kv,
             block_table=self.block_table, page=self.spec.page,
             gate=self.gate if gate else None, packed=packed, skip_topk=skip_topk,
-            rows_to_score=rows_to_score)
+            rows_to_score=rows_to_score, k_scale=self.kv_scales[0], v_scale=self.kv_scales[1])
 
     def compress(self):
         return O.compress_stage(

@@ -64,6 +64,17 @@ MID = {
                                compress_ratio=4, token_topk=256, hq=16, hkv=4, page=32),
     "small_group3": W.small_spec("small_group3", seed=22, hq=6, hkv=2),
     "small_group1": W.small_spec("small_group1", seed=23, hq=4, hkv=4),
+    # FP8-e4m3 main KV cache with static scales
+    "mid_fp8kv_r4": W.small_spec("mid_fp8kv_r4", seed=25, contexts=(2999, 4096, 300, 1500),
+                                 rows_per_req=(1, 2, 1, 4), n_heads=32, index_dtype=E4,
+                                 compress_ratio=4, token_topk=512, hq=32, hkv=4, page=64,
+                                 kv_dtype=E4, kv_scale=0.0625),
+    "mid_fp8kv_group16": W.small_spec("mid_fp8kv_group16", seed=26, contexts=(2500, 801),
+                                      rows_per_req=(3, 1), n_heads=8, index_dtype=BF,
+                                      compress_ratio=8, token_topk=512, hq=32, hkv=2, page=64,
+                                      kv_dtype=E4, kv_scale=0.03),
+    "small_fp8kv_group4": W.small_spec("small_fp8kv_group4", seed=27, hq=8, hkv=2, kv_dtype=E4,
+                                       kv_scale=0.1),
 }
 
 
@@ -189,7 +200,8 @@ def test_topk_matches_oracle(ratio, topk, positions, ties):
 # ----------------------------------------------------------------- stage 4
 @pytest.mark.parametrize("name", ["tiny_bf16", "small_bf16_copy_path", "mid_e4m3_r4",
                                   "mid_h64_e4m3_r2", "mid_mrope_h8", "mid_group16", "mid_group4",
-                                  "small_group3", "small_group1"])
+                                  "small_group3", "small_group1", "mid_fp8kv_r4",
+                                  "mid_fp8kv_group16", "small_fp8kv_group4"])
 @pytest.mark.parametrize("gate", [True, False])
 def test_sparse_gqa_matches_oracle(name, gate):
     spec = MID[name]
@@ -211,7 +223,7 @@ def test_sparse_gqa_matches_oracle(name, gate):
         n = int(packed_np[row, -1])
         req = int(st.token_to_req[row])
         want = O.sparse_gqa_row(st.q[row], st.kv, st.block_table[req], packed_np[row, :n],
-                                spec.page, st.gate[row] if gate else None)
+                                spec.page, st.gate[row] if gate else None, *st.kv_scales)
         ok, err = close_bf16(got[row], want)
         assert ok, f"row {row} (n={n}): max err {err:.3g}"
     assert (got[-1] == 0).all()
@@ -304,10 +316,10 @@ def _full_chain(spec, wl, st, step, rows=None, packed_ref=None, skip=False):
         n = int(opack[-1])
         if st.kv is not None:
             want = O.sparse_gqa_row(st.q[row], st.kv, st.block_table[req], opack[:n], spec.page,
-                                    st.gate[row])
+                                    st.gate[row], *st.kv_scales)
         else:
             want = oracle_gqa_row(st.q[row], step.wl["kv"], st.block_table[req], opack[:n],
-                                  spec.page, st.gate[row])
+                                  spec.page, st.gate[row], st.kv_scales)
         ok, err = close_bf16(got_out[row], want)
         assert ok, f"{spec.name} row {row}: output err {err:.3g}"
     return tie_rows
