@@ -48,6 +48,13 @@ R11 1-D RoPE (all sections 0): the query uses positions[row, 0, 0]; a
 R12 e4m3: round to nearest even, saturate to +-448 (OCP FP8 E4M3FN), never
     NaN.  bf16: round to nearest even.
 R13 gate: out = bf16(bf16(attn) * sigmoid(gate)); no gate: bf16(attn).
+R16 main-attention prepare (the fused qsa_prepare of QSAIndexer.forward):
+    the projection row is [Hq heads x (q | gate), Hkv heads x k, Hkv heads
+    x v], each piece head_dim wide (the sigmoid gate packed next to each
+    query head); q and k take Gemma RMSNorm (q_norm / k_norm) per head, then
+    the indexer's rotary embedding at the row's position, and are rounded
+    once (q to bf16, k to the cache dtype); the gate is passed through for
+    stage 4's sigmoid; v is stored as is (bf16) or as e4m3(v / v_scale).
 R15 FP8 main KV cache: stored value e4m3(x / scale) with a static scalar
     scale per tensor (k_scale for K, v_scale for V); attention reads the
     stored values unscaled, multiplies each score by k_scale (with
@@ -362,6 +369,51 @@ def compress_stage(cfg: QsaConfig, *, projected_q, raw_keys, positions, cos_sin,
     return q_idx, written
 
 
+def prepare_main_row(cfg: QsaConfig, qkv_row, pos3, cos_sin, q_norm_w, k_norm_w, eps: float,
+                     hq: int, hkv: int):
+    """Main-attention prepare of one row (R16): returns (q [Hq, D] bf16 values,
+    gate [Hq, D], k [Hkv, D] unrounded, v [Hkv, D]).
+
+    Follows "vllm.models.qwen4_exp.nvidia.qsa": Qwen4ExpQSAAttention.__init__
+    (qkv_proj packs the output gate next to Q: total_num_heads * (1 +
+    attn_output_gate) query-sized heads, then the K and V heads; q_norm and
+    k_norm are GemmaRMSNorm(head_dim); the indexer shares rotary_emb) and
+    QSAIndexer.forward (qsa_prepare with main_qkv, main_q_norm_weight,
+    main_k_norm_weight, main_eps: the main QK-norm/RoPE/gate in the same
+    launch as the indexer prepare).
+    """
+    D = cfg.head_dim
+    x = np.asarray(qkv_row, dtype=np.float64)
+    qg = x[: 2 * hq * D].reshape(hq, 2, D)
+    q, gate = qg[:, 0], qg[:, 1]
+    k = x[2 * hq * D: 2 * hq * D + hkv * D].reshape(hkv, D)
+    v = x[2 * hq * D + hkv * D: 2 * hq * D + 2 * hkv * D].reshape(hkv, D)
+    q = round_bf16(rope_neox(gemma_rmsnorm(q, q_norm_w, eps), pos3, cos_sin, cfg.rotary_dim,
+                             cfg.mrope_section))
+    k = rope_neox(gemma_rmsnorm(k, k_norm_w, eps), pos3, cos_sin, cfg.rotary_dim,
+                  cfg.mrope_section)
+    return q, gate.copy(), k, v.copy()
+
+
+def write_main_kv(kv, slot: int, k, v, page: int, kv_dtype: int = DTYPE_BF16,
+                  k_scale: float = 1.0, v_scale: float = 1.0) -> None:
+    """The main K/V cache write of one row (R16, R15) at flat slot
+    block * page + offset ("vllm.models.qwen4_exp.nvidia.qsa",
+    Qwen4ExpQSAImpl.do_kv_cache_update: reshape_and_cache_flash at
+    slot_mapping with the layer's scales).  kv: [blocks, Hkv, page, 2D]
+    (values; mutated)."""
+    if slot < 0:
+        return
+    D = kv.shape[-1] // 2
+    blk, off = slot // page, slot % page
+    if kv_dtype == DTYPE_E4M3:
+        kv[blk, :, off, :D] = quantize_kv_e4m3(k, k_scale)
+        kv[blk, :, off, D:] = quantize_kv_e4m3(v, v_scale)
+    else:
+        kv[blk, :, off, :D] = round_bf16(k)
+        kv[blk, :, off, D:] = round_bf16(v)
+
+
 # ---------------------------------------------------------------------------
 # Stage 2: index logits; stage 3: block top-k and expand
 # ---------------------------------------------------------------------------
@@ -503,14 +555,18 @@ def layer_step(cfg: QsaConfig, *, projected_q, raw_keys, positions, cos_sin,
                token_to_req, query_start_loc, logical_positions, ccache,
                compressed_slots, cblock_table, q, kv, block_table, page,
                gate=None, packed=None, skip_topk=False, rows_to_score=None,
-               k_scale=1.0, v_scale=1.0):
+               k_scale=1.0, v_scale=1.0, main=None):
     """O1..O7 in order: stage 1 on every row, then (unless skip_topk) stages
     2-3, then stage 4.  With skip_topk the given ``packed`` buffer (from the
     step that selected) feeds stage 4 unchanged (QSAIndexer.skip_topk:
     "later steps reuse them while continuing to update the QSA indexer
     cache").  Mutates the caches; returns (q_idx, packed, out).
     ``rows_to_score`` restricts stages 2-4 to a subset of rows (the others
-    keep packed = inert and out = 0).
+    keep packed = inert and out = 0).  ``main`` (optional) is the fused
+    main-attention prepare (R16): a dict with qkv [rows, (2Hq + 2Hkv) D],
+    q_norm_w, k_norm_w, eps, slot_mapping [rows], kv_dtype; its q and gate
+    replace ``q`` / ``gate`` and its K/V rows are written into ``kv`` before
+    stage 4.
     """
     rows = len(token_to_req)
     q_idx, _ = compress_stage(
@@ -521,6 +577,16 @@ def layer_step(cfg: QsaConfig, *, projected_q, raw_keys, positions, cos_sin,
         logical_positions=logical_positions, ccache=ccache,
         compressed_slots=compressed_slots)
     todo = range(rows) if rows_to_score is None else rows_to_score
+    if main is not None:
+        hq, hkv = q.shape[1], kv.shape[1]
+        q = np.zeros((rows, hq, cfg.head_dim))
+        gate = np.zeros((rows, hq, cfg.head_dim))
+        for row in range(rows):
+            q[row], gate[row], k, v = prepare_main_row(
+                cfg, main["qkv"][row], positions[row], cos_sin, main["q_norm_w"],
+                main["k_norm_w"], main["eps"], hq, hkv)
+            write_main_kv(kv, int(main["slot_mapping"][row]), k, v, page,
+                          main.get("kv_dtype", DTYPE_BF16), k_scale, v_scale)
     if skip_topk:
         if packed is None:
             raise ValueError("skip_topk needs the packed buffer of the selecting step")

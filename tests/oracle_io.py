@@ -59,7 +59,7 @@ class OracleState:
         self.kv_scales = ((s.kv_scale, s.kv_scale) if getattr(s, "kv_dtype", 0) == 1
                           else (1.0, 1.0))
 
-    def step(self, skip_topk=False, packed=None, rows_to_score=None, gate=True):
+    def step(self, skip_topk=False, packed=None, rows_to_score=None, gate=True, main=None):
         return O.layer_step(
             self.cfg, projected_q=self.projected_q, raw_keys=self.raw_keys,
             positions=self.positions, cos_sin=self.cos_sin, q_norm_w=self.q_norm_w,
@@ -70,7 +70,8 @@ class OracleState:
             cblock_table=self.cblock_table, q=self.q, kv=self.kv,
             block_table=self.block_table, page=self.spec.page,
             gate=self.gate if gate else None, packed=packed, skip_topk=skip_topk,
-            rows_to_score=rows_to_score, k_scale=self.kv_scales[0], v_scale=self.kv_scales[1])
+            rows_to_score=rows_to_score, k_scale=self.kv_scales[0], v_scale=self.kv_scales[1],
+            main=main)
 
     def compress(self):
         return O.compress_stage(

@@ -81,3 +81,28 @@ def test_empty_batch():
         cblock_table=np.zeros((1, 1), int), q=np.zeros((0, 8, 128)),
         kv=np.zeros((1, 1, 16, 256)), block_table=np.zeros((1, 1), int), page=16)
     assert packed.shape == (0, cfg.packed_width) and out.shape == (0, 8, 128)
+
+
+def test_within_budget_step_with_main_prepare_equals_dense_attention():
+    """With the fused main-attention prepare the step's own K/V rows are
+    written into the cache before stage 4, and its q and gate come from the
+    projection: a within-budget step then equals dense causal attention of
+    the prepared q over the cache with those rows in place."""
+    spec = W.small_spec(contexts=(12, 40, 64, 3), rows_per_req=(1, 3, 2, 1), hq=8, hkv=2)
+    st = OracleState(W.make_workload(spec))
+    rng = np.random.default_rng(3)
+    D, hq, hkv = 128, spec.hq, spec.hkv
+    qkv = O.round_bf16(rng.standard_normal((spec.rows, (2 * hq + 2 * hkv) * D)))
+    slots = np.array([int(st.block_table[int(st.token_to_req[r])][int(st.logical_positions[r]) // spec.page])
+                      * spec.page + int(st.logical_positions[r]) % spec.page for r in range(spec.rows)])
+    wq, wk = rng.standard_normal(D) * 0.1, rng.standard_normal(D) * 0.1
+    main = dict(qkv=qkv, q_norm_w=wq, k_norm_w=wk, eps=1e-6, slot_mapping=slots)
+    _, packed, out = st.step(main=main)
+    for row in range(spec.rows):
+        q, gate, k, v = O.prepare_main_row(st.cfg, qkv[row], st.positions[row], st.cos_sin, wq, wk,
+                                           1e-6, hq, hkv)
+        blk, off = slots[row] // spec.page, slots[row] % spec.page
+        np.testing.assert_array_equal(st.kv[blk, :, off, :D], O.round_bf16(k))
+        np.testing.assert_array_equal(st.kv[blk, :, off, D:], v)
+        st.q[row], st.gate[row] = q, gate
+        np.testing.assert_allclose(out[row], _dense_reference(st, row), atol=1e-2, rtol=1e-2)

@@ -593,3 +593,74 @@ def test_fp8_kv_all_selected_equals_dense_sdpa_on_dequantized_cache():
     v = torch.from_numpy(rows[..., 128:] * vs).permute(1, 0, 2).repeat_interleave(4, 0)
     ref = F.scaled_dot_product_attention(torch.from_numpy(q)[:, None, :], k, v)[:, 0].numpy()
     np.testing.assert_array_equal(got, O.round_bf16(ref))
+
+
+# --------------------------------------------------------------------------
+# Main-attention prepare (reading R16)
+# --------------------------------------------------------------------------
+
+def test_prepare_main_layout_hand_worked():
+    """Each piece of the projection row lands where reading R16 puts it: per
+    query head [q | gate], then the K heads, then the V heads.  Pieces hold
+    distinct constants (a constant vector c has RMS |c|, so Gemma RMSNorm
+    with w = 0 maps it to sign(c) everywhere, and RoPE at position 0 is the
+    identity), so a swapped or shifted slice shows up directly."""
+    hq, hkv, D = 3, 2, 128
+    cfg = _cfg(n_heads=4, eps=0.0)
+    cs = _table()
+    x = np.zeros((2 * hq + 2 * hkv) * D)
+    consts = {}
+    for h in range(hq):
+        x[(2 * h) * D:(2 * h + 1) * D] = -(h + 1.0)           # q of head h (negative)
+        x[(2 * h + 1) * D:(2 * h + 2) * D] = 10.0 + h         # gate of head h
+        consts[("gate", h)] = 10.0 + h
+    for h in range(hkv):
+        x[(2 * hq + h) * D:(2 * hq + h + 1) * D] = 5.0 + h    # k of head h
+        x[(2 * hq + hkv + h) * D:(2 * hq + hkv + h + 1) * D] = 20.0 + h  # v of head h
+    q, gate, k, v = O.prepare_main_row(cfg, x, (0, 0, 0), cs, np.zeros(D), np.zeros(D), 0.0,
+                                       hq, hkv)
+    np.testing.assert_array_equal(q, -np.ones((hq, D)))
+    np.testing.assert_array_equal(gate, np.array([[10.0 + h] * D for h in range(hq)]))
+    np.testing.assert_allclose(k, np.ones((hkv, D)), atol=1e-15)
+    np.testing.assert_array_equal(v, np.array([[20.0 + h] * D for h in range(hkv)]))
+
+
+def test_prepare_main_norm_then_rope_matches_independent_restatement():
+    """q and k: Gemma RMSNorm (torch rms_norm with 1 + w) per head, then
+    RoPE as a complex rotation at the row's MRoPE position; q rounded once
+    to bf16."""
+    hq, hkv, D = 4, 2, 128
+    cfg = _cfg(n_heads=4, eps=1e-6, mrope_section=(8, 12, 12))
+    cs = _table()
+    comps = _golden_components()
+    x = RNG.standard_normal((2 * hq + 2 * hkv) * D)
+    wq, wk = RNG.standard_normal(D) * 0.1, RNG.standard_normal(D) * 0.1
+    pos = (17, 900, 2100)
+    q, gate, k, v = O.prepare_main_row(cfg, x, pos, cs, wq, wk, 1e-6, hq, hkv)
+    qg = x[: 2 * hq * D].reshape(hq, 2, D)
+    want_q = _rope_complex(_norm(qg[:, 0], wq, 1e-6), pos, comps)
+    _within_one_bf16_step(q, want_q)
+    kk = x[2 * hq * D: (2 * hq + hkv) * D].reshape(hkv, D)
+    np.testing.assert_allclose(k, _rope_complex(_norm(kk, wk, 1e-6), pos, comps), atol=1e-12)
+    np.testing.assert_array_equal(gate, qg[:, 1])
+
+
+def test_write_main_kv_slot_and_dtypes():
+    """The row's K/V go to block slot // page, offset slot % page, every KV
+    head, K then V; bf16 rounding or e4m3(x / scale); slot < 0 writes
+    nothing."""
+    kv = np.zeros((5, 2, 16, 256))
+    k = RNG.standard_normal((2, 128))
+    v = RNG.standard_normal((2, 128))
+    O.write_main_kv(kv, 3 * 16 + 9, k, v, 16)
+    np.testing.assert_array_equal(kv[3, :, 9, :128], O.round_bf16(k))
+    np.testing.assert_array_equal(kv[3, :, 9, 128:], O.round_bf16(v))
+    assert np.count_nonzero(kv) == np.count_nonzero(kv[3, :, 9])
+    kv8 = np.zeros((5, 2, 16, 256))
+    O.write_main_kv(kv8, 17, k, v, 16, O.DTYPE_E4M3, 0.05, 0.02)
+    want_k = torch.from_numpy((k / 0.05).astype(np.float32)).to(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(kv8[1, :, 1, :128], want_k)
+    np.testing.assert_array_equal(kv8[1, :, 1, 128:], O.quantize_kv_e4m3(v, 0.02))
+    before = kv8.copy()
+    O.write_main_kv(kv8, -1, k, v, 16)
+    np.testing.assert_array_equal(kv8, before)
