@@ -484,7 +484,8 @@ def decode_report(name, device, steps, warmup, flush, drain, hbm):
     step (tokens/s, step against HBM) and its sparse GQA kernel alone."""
     spec = W.named_spec(name)
     wl, cfg, gcfg, mv, packed, out, ws = build(spec, device)
-    sargs = Q.step_args(wl.t, packed, out, mv)
+    main = Q.main_prep(wl.t, spec.eps) if spec.main_prep else None
+    sargs = Q.step_args(wl.t, packed, out, mv, main=main)
     for _ in range(warmup):
         Q.layer_step(cfg, gcfg, sargs, ws)
     graph = capture(lambda: Q.layer_step(cfg, gcfg, sargs, ws), device)
@@ -694,6 +695,8 @@ def run_ours(args):
                  "long_decode": decode_report("long_decode", device, 10, 3, flush, drain, hbm),
                  "decode_batch_fp8kv": decode_report("decode_batch_fp8kv", device, 10, 3, flush,
                                                      drain, hbm),
+                 "decode_batch_prepare": decode_report("decode_batch_prepare", device, 10, 3,
+                                                       flush, drain, hbm),
                  "mtp_mrope": mtp_report(device, 10, 3, flush, drain, hbm)}
 
     if rank == 0:

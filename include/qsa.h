@@ -243,6 +243,45 @@ qsa_status qsa_sparse_gqa_noalloc(const qsa_gqa_cfg* gcfg, const void* q, const 
                                   const int32_t* token_to_req, const void* gate, void* out,
                                   int32_t rows, void* stream);
 
+/*
+ * Main-attention prepare, fused into the stage-1 launch of a layer step
+ * ("vllm.models.qwen4_exp.nvidia.qsa", QSAIndexer.forward: the qsa_prepare
+ * call with main_qkv, main_q_norm_weight, main_k_norm_weight, main_eps,
+ * main_kv_cache, main_slot_mapping, main_k_scale, main_v_scale;
+ * Qwen4ExpQSAAttention.__init__: the sigmoid output gate packed next to each
+ * query head, q_norm / k_norm = GemmaRMSNorm(head_dim), the rotary embedding
+ * shared with the indexer; Qwen4ExpQSAImpl.do_kv_cache_update: the K/V write
+ * at slot_mapping).  Per row: q = RoPE(GemmaRMSNorm(q)) rounded to bf16, the
+ * gate passed through (stage 4 applies the sigmoid), k = RoPE(GemmaRMSNorm(k))
+ * and v written into the main KV cache at the row's slot (bf16, or
+ * e4m3(x / scale) with the gcfg's scales), at the positions and with the
+ * cos/sin table and MRoPE sections of the indexer.
+ *  qkv          [rows, (2*Hq + 2*Hkv) * D] bf16: per query head [q | gate],
+ *               then the Hkv K heads, then the Hkv V heads
+ *  q_norm_w, k_norm_w  [D] bf16 (scale 1 + w); eps their epsilon
+ *  q_out, gate_out     [rows, Hq, D] bf16 (out)
+ *  kv           the main KV cache [num_blocks, Hkv, page, 2*D] (written)
+ *  slot_mapping [rows] int64: block * page + offset of the row's token;
+ *               < 0 writes nothing for that row
+ */
+typedef struct qsa_main_prep {
+  const void* qkv;
+  const void* q_norm_w;
+  const void* k_norm_w;
+  float eps;
+  void* q_out;
+  void* gate_out;
+  void* kv;
+  const int64_t* slot_mapping;
+} qsa_main_prep;
+
+/* The main-attention prepare alone (one launch), for callers that run the
+ * stages one by one.  positions [rows, 1, 3] int64 and cos_sin as for
+ * qsa_compress. */
+qsa_status qsa_main_prepare(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa_main_prep* m,
+                            const int64_t* positions, const float* cos_sin, int32_t rows,
+                            void* stream);
+
 /* Arguments of one fused layer step (all device pointers; meanings as in the
  * stage calls above). */
 typedef struct qsa_step_args {
@@ -274,10 +313,15 @@ typedef struct qsa_step_args {
   int32_t bt_stride;
   const void* gate;                 /* [rows, Hq, D] bf16 or NULL */
   void* out;                        /* [rows, Hq, D] bf16 */
+  /* NULL, or the main-attention prepare to fuse into stage 1: its q_out and
+   * gate_out then feed stage 4 (q and gate above are ignored) and its kv must
+   * be this step's kv. */
+  const qsa_main_prep* main;
 } qsa_step_args;
 
 /*
- * qsa_layer_step -- stages 1 to 4 in order on one stream.
+ * qsa_layer_step -- stages 1 to 4 in order on one stream (with args->main,
+ * stage 1 also prepares the main attention's q, gate and K/V cache rows).
  * Follows "vllm.models.qwen4_exp.nvidia.qsa", Qwen4ExpQSAAttention._run_qsa
  * and QSAIndexer.forward.  With skip_topk != 0 (MTP steps after step 0,
  * QSAIndexer.skip_topk) stage 1 still updates the ring and the compressed

@@ -152,6 +152,37 @@ qsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_E
 
 size_t topk_limit_bytes() { return 220 * 1024; }
 
+// Checks the main-attention prepare's arguments and adds them to p (whose
+// positions, cos/sin table and RoPE layout it shares).
+qsa_status fill_main(CompressParams* p, const qsa_gqa_cfg* g, const qsa_main_prep* m) {
+  const qsa_status st = check_gcfg(g);
+  if (st != QSA_OK) return st;
+  if (!m->qkv || !m->q_norm_w || !m->k_norm_w || !m->q_out || !m->gate_out || !m->kv ||
+      !m->slot_mapping)
+    return QSA_ERR_INVALID_ARG;
+  if (!(m->eps >= 0.f)) return QSA_ERR_INVALID_ARG;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(m->qkv) | reinterpret_cast<uintptr_t>(m->q_norm_w) |
+                        reinterpret_cast<uintptr_t>(m->k_norm_w) | reinterpret_cast<uintptr_t>(m->q_out) |
+                        reinterpret_cast<uintptr_t>(m->gate_out) | reinterpret_cast<uintptr_t>(m->kv);
+  if (a16 & 15) return QSA_ERR_INVALID_ARG;
+  p->main_qkv = static_cast<const uint16_t*>(m->qkv);
+  p->main_q_norm_w = static_cast<const uint16_t*>(m->q_norm_w);
+  p->main_k_norm_w = static_cast<const uint16_t*>(m->k_norm_w);
+  p->main_eps = m->eps;
+  p->main_q_out = static_cast<uint16_t*>(m->q_out);
+  p->main_gate_out = static_cast<uint16_t*>(m->gate_out);
+  p->main_kv = m->kv;
+  p->main_slots = m->slot_mapping;
+  p->main_hq = g->num_q_heads;
+  p->main_hkv = g->num_kv_heads;
+  p->main_page = g->page_size;
+  p->main_blocks = g->num_blocks;
+  p->main_kv_dtype = g->kv_dtype;
+  p->main_k_scale = g->k_scale;
+  p->main_v_scale = g->v_scale;
+  return QSA_OK;
+}
+
 qsa_status do_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
                        const void* raw_keys, const int64_t* positions, const float* cos_sin,
                        const void* q_norm_w, const void* k_norm_w, void* ring, int32_t ring_blocks,
@@ -160,7 +191,8 @@ qsa_status do_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
                        const int32_t* logical_positions, void* ccache, int32_t cpages,
                        const int64_t* compressed_slots, int32_t rows, int32_t reqs,
                        cudaStream_t stream, bool commit_ring = true,
-                       CompressParams* out_params = nullptr) {
+                       CompressParams* out_params = nullptr,
+                       const qsa_gqa_cfg* gcfg = nullptr, const qsa_main_prep* main = nullptr) {
   qsa_status st = check_cfg(cfg);
   if (st != QSA_OK) return st;
   if (rows < 0 || reqs < 0) return QSA_ERR_SHAPE;
@@ -212,6 +244,10 @@ qsa_status do_compress(const qsa_cfg* cfg, const void* projected_q, void* q_idx,
   p.eps = cfg->eps;
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
+  if (main != nullptr) {
+    st = fill_main(&p, gcfg, main);
+    if (st != QSA_OK) return st;
+  }
   if (out_params != nullptr) *out_params = p;
   if (t_validate_only) return QSA_OK;
   st = cuda_status(launch_compress(p, stream, /*pdl=*/false));
@@ -366,7 +402,7 @@ qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
                   const int32_t* block_table, int32_t bt_stride, const int32_t* packed,
                   int32_t packed_width, const int32_t* token_to_req, const void* gate, void* out,
                   int32_t rows, void* ws, size_t ws_bytes, cudaStream_t stream,
-                  bool pdl = false, bool tickets_zeroed = false) {
+                  bool pdl = false, bool tickets_zeroed = false, bool q_after_wait = false) {
   qsa_status st = check_gcfg(gcfg);
   if (st != QSA_OK) return st;
   if (rows < 0) return QSA_ERR_SHAPE;
@@ -382,6 +418,7 @@ qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
   p.kv_dtype = gcfg->kv_dtype;
   p.k_scale = gcfg->k_scale;
   p.v_scale = gcfg->v_scale;
+  p.q_after_wait = q_after_wait ? 1 : 0;
   p.block_table = block_table;
   p.packed = packed;
   p.token_to_req = token_to_req;
@@ -539,6 +576,11 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int pw = cfg->token_topk + cfg->compress_ratio;
+  // stage 4's query and gate: the caller's, or the fused prepare's
+  const qsa_main_prep* mp = a->main;
+  if (mp != nullptr && mp->kv != a->kv) return QSA_ERR_INVALID_ARG;
+  const void* q4 = mp != nullptr ? mp->q_out : a->q;
+  const void* gate4 = mp != nullptr ? mp->gate_out : a->gate;
   const GqaLayout G = gqa_layout(gcfg, a->rows, pw);
   // Kernels after the first start early (programmatic dependent launch) and
   // wait on the device for their predecessor's results.
@@ -547,11 +589,12 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
     st = do_compress(cfg, nullptr, nullptr, a->raw_keys, a->positions, a->cos_sin, a->q_norm_w,
                      a->k_norm_w, a->ring, a->ring_blocks, a->ring_pos, a->ring_block_table,
                      a->ring_bt_stride, a->token_to_req, a->query_start_loc, a->logical_positions,
-                     a->ccache, a->cpages, a->compressed_slots, a->rows, a->reqs, s);
+                     a->ccache, a->cpages, a->compressed_slots, a->rows, a->reqs, s,
+                     /*commit_ring=*/true, nullptr, gcfg, mp);
     if (st != QSA_OK) return st;
-    return do_gqa(gcfg, a->q, a->kv, a->block_table, a->bt_stride, a->packed, pw,
-                  a->token_to_req, a->gate, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s,
-                  /*pdl=*/true, /*tickets_zeroed=*/false);
+    return do_gqa(gcfg, q4, a->kv, a->block_table, a->bt_stride, a->packed, pw,
+                  a->token_to_req, gate4, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s,
+                  /*pdl=*/true, /*tickets_zeroed=*/false, /*q_after_wait=*/mp != nullptr);
   }
   void* q_idx = w + L.q_idx;
   float* logits = reinterpret_cast<float*>(w + L.logits);
@@ -570,7 +613,7 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
                    a->q_norm_w, a->k_norm_w, a->ring, a->ring_blocks, a->ring_pos,
                    a->ring_block_table, a->ring_bt_stride, a->token_to_req, a->query_start_loc,
                    a->logical_positions, a->ccache, a->cpages, a->compressed_slots, a->rows,
-                   a->reqs, s, /*commit_ring=*/false, &cp);
+                   a->reqs, s, /*commit_ring=*/false, &cp, gcfg, mp);
   if (st != QSA_OK) return st;
   if (any_visible && !t_validate_only) {
     st = launch_logits(cfg, lp, q_idx, a->rows, npad, chunks, groups, /*pdl=*/true, s);
@@ -583,9 +626,32 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
   st = do_topk(cfg, logits, L.ld, a->max_visible, a->logical_positions, a->packed, a->rows, s, &cp,
                tickets, tickets ? gcfg->num_kv_heads : 0, /*pdl=*/any_visible);
   if (st != QSA_OK) return st;
-  return do_gqa(gcfg, a->q, a->kv, a->block_table, a->bt_stride, a->packed, pw, a->token_to_req,
-                a->gate, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s, /*pdl=*/true,
-                /*tickets_zeroed=*/tickets != nullptr);
+  return do_gqa(gcfg, q4, a->kv, a->block_table, a->bt_stride, a->packed, pw, a->token_to_req,
+                gate4, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s, /*pdl=*/true,
+                /*tickets_zeroed=*/tickets != nullptr, /*q_after_wait=*/mp != nullptr);
+}
+
+qsa_status qsa_main_prepare(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa_main_prep* m,
+                            const int64_t* positions, const float* cos_sin, int32_t rows,
+                            void* stream) {
+  qsa_status st = check_cfg(cfg);
+  if (st != QSA_OK) return st;
+  if (m == nullptr || rows < 0) return rows < 0 ? QSA_ERR_SHAPE : QSA_ERR_INVALID_ARG;
+  if (rows == 0) return QSA_OK;
+  if (!positions || !cos_sin) return QSA_ERR_INVALID_ARG;
+  CompressParams p{};
+  p.positions = positions;
+  p.cos_sin = cos_sin;
+  p.rows = rows;
+  p.max_pos = cfg->max_position;
+  p.mrope = (cfg->mrope_section[0] || cfg->mrope_section[1] || cfg->mrope_section[2]) ? 1 : 0;
+  p.sec_h = cfg->mrope_section[1];
+  p.sec_w = cfg->mrope_section[2];
+  st = fill_main(&p, gcfg, m);
+  if (st != QSA_OK) return st;
+  p.err = error_word();
+  if (p.err == nullptr) return QSA_ERR_CUDA;
+  return cuda_status(launch_main_prepare(p, static_cast<cudaStream_t>(stream)));
 }
 
 qsa_status qsa_mtp_steps(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa_step_args* steps,

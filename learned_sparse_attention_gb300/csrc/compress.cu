@@ -14,7 +14,9 @@
 // row i: 8 half-warps, each owning n_heads / 8 head vectors, each lane 8
 // consecutive dims (one 16-byte load per head, all issued before any math);
 // RoPE partners (i, i + 32) sit 4 lanes apart.  CTA rows + i pools the group
-// completed by row i, if any, in parallel with the query CTAs.
+// completed by row i, if any, in parallel with the query CTAs.  With the fused
+// main-attention prepare, CTA 2 rows + i prepares row i's main q, gate and
+// K/V cache rows (caller inputs only, so it does not wait for anything).
 #include "qsa_device.cuh"
 #include "qsa_kernels.h"
 #include "qsa_launch.cuh"
@@ -45,9 +47,96 @@ __device__ __forceinline__ void store8(void* base, long long elem_off, const flo
   }
 }
 
+// Main-attention prepare of one row by a 128-thread CTA (8 half-warps, each
+// a 128-dim head vector, 8 dims per lane): q = RoPE(GemmaRMSNorm(q)) -> bf16,
+// the gate passed through, k = RoPE(GemmaRMSNorm(k)) and v written into the
+// paged KV cache at the row's slot (bf16, or e4m3(x / scale)).  Follows
+// "vllm.models.qwen4_exp.nvidia.qsa", QSAIndexer.forward (the qsa_prepare
+// call: main_qkv, main_q_norm_weight, main_k_norm_weight, main_eps,
+// main_kv_cache, main_slot_mapping, main_k_scale, main_v_scale) and
+// Qwen4ExpQSAAttention.__init__ (the gate packed next to each query head,
+// q_norm / k_norm per head, the indexer's rotary embedding).
+__device__ __forceinline__ void main_prepare_row(const CompressParams& P, int row) {
+  const int hw = threadIdx.x >> 4, lane16 = threadIdx.x & 15;
+  const int HQ = P.main_hq, HKV = P.main_hkv;
+  const uint16_t* x = P.main_qkv + static_cast<long long>(row) * (2 * HQ + 2 * HKV) * kD;
+  int64_t pos[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) pos[k] = P.positions[static_cast<long long>(row) * 3 + (P.mrope ? k : 0)];
+  float c[8], s[8], wq[8], wk[8];
+  rope_coeffs(rope_params(P), lane16, pos, c, s);
+  load8_bf16(P.main_q_norm_w + 8 * lane16, wq);
+  load8_bf16(P.main_k_norm_w + 8 * lane16, wk);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    wq[e] += 1.0f;
+    wk[e] += 1.0f;
+  }
+  // query heads (both half-warps of a warp run the same iterations: the
+  // norm's shuffles span the warp)
+  for (int base = 0; base < HQ; base += 8) {
+    const int h = base + hw;
+    const bool act = h < HQ;
+    float xq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    uint4 gv = make_uint4(0u, 0u, 0u, 0u);
+    if (act) {
+      load8_bf16(x + (2 * h) * kD + 8 * lane16, xq);
+      gv = *reinterpret_cast<const uint4*>(x + (2 * h + 1) * kD + 8 * lane16);
+    }
+    norm_rope(xq, wq, P.main_eps, lane16, c, s);
+    if (act) {
+      const long long o = (static_cast<long long>(row) * HQ + h) * kD + 8 * lane16;
+      store8<0>(P.main_q_out, o, xq);
+      *reinterpret_cast<uint4*>(P.main_gate_out + o) = gv;
+    }
+  }
+  // K and V into the cache at the row's slot
+  const long long slot = P.main_slots[row];
+  if (slot < 0) return;
+  const long long blk = slot / P.main_page, off = slot - blk * P.main_page;
+  if (blk >= P.main_blocks) {
+    if (threadIdx.x == 0) flag_error(P.err);
+    return;
+  }
+  for (int base = 0; base < HKV; base += 8) {
+    const int h = base + hw;
+    const bool act = h < HKV;
+    float xk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    uint4 vv = make_uint4(0u, 0u, 0u, 0u);
+    if (act) {
+      load8_bf16(x + (2 * HQ + h) * kD + 8 * lane16, xk);
+      vv = *reinterpret_cast<const uint4*>(x + (2 * HQ + HKV + h) * kD + 8 * lane16);
+    }
+    norm_rope(xk, wk, P.main_eps, lane16, c, s);
+    if (!act) continue;
+    const long long r = (blk * HKV + h) * P.main_page + off;  // (token, KV head) row
+    if (P.main_kv_dtype == 0) {
+      uint16_t* dst = static_cast<uint16_t*>(P.main_kv) + r * 256;
+      store8<0>(dst, 8 * lane16, xk);
+      *reinterpret_cast<uint4*>(dst + 128 + 8 * lane16) = vv;
+    } else {
+      uint8_t* dst = static_cast<uint8_t*>(P.main_kv) + r * 256;
+      const float ik = 1.0f / P.main_k_scale, iv = 1.0f / P.main_v_scale;
+      float xv[8] = {bf16_lo(vv.x), bf16_hi(vv.x), bf16_lo(vv.y), bf16_hi(vv.y),
+                     bf16_lo(vv.z), bf16_hi(vv.z), bf16_lo(vv.w), bf16_hi(vv.w)};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        xk[e] *= ik;
+        xv[e] *= iv;
+      }
+      store8<1>(dst, 8 * lane16, xk);
+      store8<1>(dst, 128 + 8 * lane16, xv);
+    }
+  }
+}
+
 template <int IDT>
 __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
   griddep_launch_dependents();
+  if (blockIdx.x >= 2 * P.rows) {  // reads only caller inputs: no wait
+    main_prepare_row(P, blockIdx.x - 2 * P.rows);
+    return;
+  }
   griddep_wait();
   const int b = blockIdx.x;
   const bool pool = b >= P.rows;
@@ -160,13 +249,23 @@ __global__ void __launch_bounds__(128) ring_commit_kernel(const CompressParams P
   if (row < P.rows) ring_commit_row(P, row, threadIdx.x & 15);
 }
 
+__global__ void __launch_bounds__(128) main_prepare_kernel(const CompressParams P) {
+  main_prepare_row(P, blockIdx.x);
+}
+
 }  // namespace
 
 cudaError_t launch_compress(const CompressParams& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
+  const int grid = (p.main_qkv != nullptr ? 3 : 2) * p.rows;
   if (p.index_dtype == 1)
-    return launch_kernel(compress_kernel<1>, dim3(2 * p.rows), dim3(128), 0, stream, pdl, p);
-  return launch_kernel(compress_kernel<0>, dim3(2 * p.rows), dim3(128), 0, stream, pdl, p);
+    return launch_kernel(compress_kernel<1>, dim3(grid), dim3(128), 0, stream, pdl, p);
+  return launch_kernel(compress_kernel<0>, dim3(grid), dim3(128), 0, stream, pdl, p);
+}
+
+cudaError_t launch_main_prepare(const CompressParams& p, cudaStream_t stream) {
+  if (p.rows == 0) return cudaSuccess;
+  return launch_kernel(main_prepare_kernel, dim3(p.rows), dim3(128), 0, stream, false, p);
 }
 
 cudaError_t launch_ring_commit(const CompressParams& p, cudaStream_t stream, bool pdl) {

@@ -36,11 +36,26 @@ struct CompressParams {
   int index_dtype, mrope, sec_h, sec_w;
   float eps;
   unsigned long long* err;
+  // fused main-attention prepare (main_qkv == null: none)
+  const uint16_t* main_qkv;     // [rows, (2 Hq + 2 Hkv) * 128] bf16
+  const uint16_t* main_q_norm_w;
+  const uint16_t* main_k_norm_w;
+  float main_eps;
+  uint16_t* main_q_out;         // [rows, Hq, 128] bf16
+  uint16_t* main_gate_out;      // [rows, Hq, 128] bf16
+  void* main_kv;                // [blocks, Hkv, page, 256] bf16 or e4m3
+  const int64_t* main_slots;    // [rows] block * page + offset, < 0: no write
+  int main_hq, main_hkv, main_page, main_blocks, main_kv_dtype;
+  float main_k_scale, main_v_scale;
 };
 
 // pdl: launch with programmatic dependent launch (the kernel waits for the
 // previous kernel on the stream before touching its results).
+// With p.main_qkv set, the launch also prepares the main attention's q, gate
+// and K/V cache rows (one more CTA per row).
 cudaError_t launch_compress(const CompressParams& p, cudaStream_t stream, bool pdl);
+// The main-attention prepare alone (one CTA per row).
+cudaError_t launch_main_prepare(const CompressParams& p, cudaStream_t stream);
 cudaError_t launch_ring_commit(const CompressParams& p, cudaStream_t stream, bool pdl);
 
 struct LogitsParams {
@@ -101,6 +116,7 @@ struct GqaParams {
   int rows, hq, hkv, group, page, num_blocks, splits;  // group = hq / hkv: 1..8 or 16
   int kv_dtype;            // 0: bf16, 1: e4m3 with static scales
   float k_scale, v_scale;  // e4m3: stored value * scale = cached value
+  int q_after_wait;        // q and gate are written by the kernels before this one
   unsigned long long* err;
 };
 // Split-KV factor for `rows` rows on a device with `sms` multiprocessors.

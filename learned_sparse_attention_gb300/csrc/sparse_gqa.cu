@@ -151,8 +151,10 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   const int32_t* prow = P.packed + static_cast<long long>(row) * P.packed_width;
   // Q^T fragments (B operand of S^T = K.Q^T): head kvh * G + 8 nb + g (zero
   // past the group), 2 dims per register; a caller input, loaded before
-  // waiting for the top-k kernel.
+  // waiting for the top-k kernel (after it when the same layer step's
+  // main-attention prepare writes q and the gate).
   uint32_t qb[NB][8][2];
+  auto load_q = [&]() {
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
     const int hl = nb * 8 + g;
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
       }
     }
   }
+  };
   // The request's block-table row (a caller input) is copied before the
   // wait into the last pipeline stage of all warps (contiguous, and not
   // written before the main loop), so that resolving the selected tokens'
@@ -195,13 +198,23 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   // the group, 8 dims) and their gate (a caller input)
   const int d0 = (threadIdx.x & 15) * 8;   // 8 dims per item
   uint4 gate8[NB];
+  auto load_gates = [&]() {
 #pragma unroll
-  for (int nb = 0; nb < NB; ++nb) {
-    const int hh = (threadIdx.x + kThreads * nb) >> 4;
-    gate8[nb] = hh < G ? load_gate8(P, (static_cast<long long>(row) * P.hq + kvh * G + hh) * 128 + d0)
-                       : make_uint4(0u, 0u, 0u, 0u);
+    for (int nb = 0; nb < NB; ++nb) {
+      const int hh = (threadIdx.x + kThreads * nb) >> 4;
+      gate8[nb] = hh < G ? load_gate8(P, (static_cast<long long>(row) * P.hq + kvh * G + hh) * 128 + d0)
+                         : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if (!P.q_after_wait) {
+    load_q();
+    load_gates();
   }
   griddep_wait();  // the packed selection (and merge tickets) are written
+  if (P.q_after_wait) {
+    load_q();
+    load_gates();
+  }
   // Without split-KV the CTA's range starts at token 0 whatever the count,
   // so its first entries (kFirst per thread, up to kFirst * kThreads tokens)
   // load together with the count: one round trip before the first copies.

@@ -45,6 +45,11 @@ class QsaGqaCfg(ctypes.Structure):
                 ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
+class QsaMainPrep(ctypes.Structure):
+    _fields_ = [("qkv", _p), ("q_norm_w", _p), ("k_norm_w", _p), ("eps", ctypes.c_float),
+                ("q_out", _p), ("gate_out", _p), ("kv", _p), ("slot_mapping", _p)]
+
+
 class QsaStepArgs(ctypes.Structure):
     _fields_ = [("rows", _c_int), ("reqs", _c_int), ("max_visible", _c_int),
                 ("projected_q", _p), ("raw_keys", _p), ("positions", _p), ("cos_sin", _p),
@@ -53,7 +58,8 @@ class QsaStepArgs(ctypes.Structure):
                 ("ccache", _p), ("cpages", _c_int), ("cblock_table", _p), ("cbt_stride", _c_int),
                 ("compressed_slots", _p), ("token_to_req", _p), ("query_start_loc", _p),
                 ("logical_positions", _p), ("packed", _p), ("q", _p), ("kv", _p),
-                ("block_table", _p), ("bt_stride", _c_int), ("gate", _p), ("out", _p)]
+                ("block_table", _p), ("bt_stride", _c_int), ("gate", _p), ("out", _p),
+                ("main", _p)]
 
 
 _LIB = None
@@ -81,6 +87,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qsa_sparse_gqa": [P, P, P, P, I, P, I, P, P, P, I, P, Z, P],
         "qsa_layer_step": [P, P, P, I, P, Z, P],
         "qsa_mtp_steps": [P, P, P, I, P, Z, P],
+        "qsa_main_prepare": [P, P, P, P, P, I, P],
         "qsa_workspace_bytes": [P, P, I, I, I],
         "qsa_status_string": [I],
         "qsa_check_errors": [ctypes.POINTER(ctypes.c_int64)],
@@ -220,9 +227,35 @@ def workspace_bytes(cfg, gcfg, rows, reqs, max_visible) -> int:
                                           max_visible))
 
 
-def step_args(t: dict, packed, out, max_visible) -> QsaStepArgs:
+def main_prep(t: dict, eps: float = 1e-6) -> QsaMainPrep:
+    """The main-attention prepare's argument struct from named CUDA tensors
+    (main_qkv, main_q_norm_w, main_k_norm_w, main_q_out, main_gate_out, kv,
+    slot_mapping) and the norms' epsilon."""
+    m = QsaMainPrep()
+    m.qkv = _ptr(t["main_qkv"], torch.bfloat16, "main_qkv")
+    m.q_norm_w = _ptr(t["main_q_norm_w"], torch.bfloat16)
+    m.k_norm_w = _ptr(t["main_k_norm_w"], torch.bfloat16)
+    m.eps = float(eps)
+    m.q_out = _ptr(t["main_q_out"], torch.bfloat16, "main_q_out")
+    m.gate_out = _ptr(t["main_gate_out"], torch.bfloat16, "main_gate_out")
+    m.kv = _ptr(t["kv"], _IDX)
+    m.slot_mapping = _ptr(t["slot_mapping"], torch.int64, "slot_mapping")
+    m._tensors = dict(t)
+    return m
+
+
+def main_prepare(cfg, gcfg, m: QsaMainPrep, positions, cos_sin, stream=None):
+    """The main-attention prepare alone (qsa_main_prepare)."""
+    st = load().qsa_main_prepare(ctypes.byref(cfg), ctypes.byref(gcfg), ctypes.byref(m),
+                                 _ptr(positions, torch.int64), _ptr(cos_sin, torch.float32),
+                                 positions.shape[0], _stream(stream))
+    _check("qsa_main_prepare", st)
+
+
+def step_args(t: dict, packed, out, max_visible, main: QsaMainPrep | None = None) -> QsaStepArgs:
     """Fill the step argument struct from named CUDA tensors (keys as produced
-    by learned_sparse_attention_gb300.workloads)."""
+    by learned_sparse_attention_gb300.workloads); `main` fuses the
+    main-attention prepare into stage 1."""
     a = QsaStepArgs()
     a.rows = t["raw_keys"].shape[0]
     a.reqs = t["query_start_loc"].shape[0] - 1
@@ -253,9 +286,10 @@ def step_args(t: dict, packed, out, max_visible) -> QsaStepArgs:
     a.bt_stride = t["block_table"].shape[1]
     a.gate = _ptr(t.get("gate"), torch.bfloat16)
     a.out = _ptr(out, torch.bfloat16)
-    # the struct holds raw device addresses: keep the tensors behind them alive
-    # for as long as the struct is
-    a._tensors = (dict(t), packed, out)
+    a.main = ctypes.addressof(main) if main is not None else None
+    # the struct holds raw device addresses: keep the tensors (and the
+    # prepare's struct) behind them alive for as long as the struct is
+    a._tensors = (dict(t), packed, out, main)
     return a
 
 

@@ -20,6 +20,9 @@ Workload recipe (all values seeded):
   gathers are not sequential;
 * RoPE cos/sin table: theta = 10000, fp32, [max_pos, rotary_dim] with cos
   in the first half and sin in the second;
+* with the main-attention prepare: the qkv projection rows ~ N(0, 1) bf16
+  ([rows, (2 Hq + 2 Hkv) * 128]), its q/k norm weights ~ N(0, 0.1), and the
+  slot of each row's own token (its block-table page and offset);
 * the "peaked" long-context workload picks a seeded 1% of each request's
   token positions and scales by 8 the raw indexer key, the main-cache K row
   and the compressed key of the group holding each of them (the prefix of
@@ -63,6 +66,7 @@ class WorkloadSpec:
     image_span: int = 0       # MRoPE image-span length per request (0 = text only)
     mtp_steps: int = 1        # steps 1.. reuse step 0's selection (skip_topk)
     state_size: int = 0       # 0 -> 2 * compress_ratio
+    main_prep: bool = False   # inputs of the fused main-attention prepare (qkv projection, slots)
     kv_dtype: int = DTYPE_BF16  # main KV cache: bf16, or e4m3 with a static scale
     kv_scale: float = 1.0 / 16  # e4m3 cache: stored value = e4m3(x / kv_scale), K and V alike
 
@@ -113,11 +117,13 @@ def named_spec(name: str) -> WorkloadSpec:
                             mrope_section=(8, 12, 12), image_span=1024, mtp_steps=4)
     if name == "decode_batch_fp8kv":  # the decode batch over an FP8-e4m3 main KV cache
         return WorkloadSpec(name, 1, _decode_contexts(1), [1] * 64, kv_dtype=DTYPE_E4M3)
+    if name == "decode_batch_prepare":  # the decode batch with the fused main-attention prepare
+        return WorkloadSpec(name, 1, _decode_contexts(1), [1] * 64, main_prep=True)
     raise KeyError(name)
 
 
 NAMED = ("tiny_bf16", "decode_batch", "chunked_prefill", "long_decode", "mtp_mrope",
-         "decode_batch_fp8kv")
+         "decode_batch_fp8kv", "decode_batch_prepare")
 
 
 def rope_cos_sin(max_pos: int, rotary_dim: int, theta: float = 10000.0) -> torch.Tensor:
@@ -263,6 +269,18 @@ def make_workload(spec: WorkloadSpec, device="cpu", step: int = 0, with_caches: 
     if ring_pos is not None:
         t["ring_pos"] = torch.from_numpy(ring_pos)
 
+    if spec.main_prep:
+        gm = torch.Generator(device="cpu").manual_seed(spec.seed * 1000 + 500 + step)
+        t["main_qkv"] = _randn(gm, (rows, (2 * spec.hq + 2 * spec.hkv) * D), "cpu")
+        gw2 = torch.Generator(device="cpu").manual_seed(spec.seed * 1000 + 501)
+        t["main_q_norm_w"] = _randn(gw2, (D,), "cpu", std=0.1)
+        t["main_k_norm_w"] = _randn(gw2, (D,), "cpu", std=0.1)
+        slot_map = np.array([int(block_table[int(token_to_req[r]), int(logical[r]) // spec.page])
+                             * spec.page + int(logical[r]) % spec.page for r in range(rows)],
+                            dtype=np.int64)
+        t["slot_mapping"] = torch.from_numpy(slot_map)
+        t["main_q_out"] = torch.zeros((rows, spec.hq, D), dtype=torch.bfloat16)
+        t["main_gate_out"] = torch.zeros((rows, spec.hq, D), dtype=torch.bfloat16)
     dev = torch.device(device)
     if not with_caches:
         t = {k: v.to(dev) for k, v in t.items() if k != "ring"}

@@ -22,6 +22,14 @@ def cfgs(spec, wl):
     return cfg, gcfg
 
 
+def oracle_main(spec, wl):
+    """The main-attention prepare's inputs as the oracle takes them (host
+    copies of the workload's generator data)."""
+    return dict(qkv=f64(wl["main_qkv"]), q_norm_w=f64(wl["main_q_norm_w"]),
+                k_norm_w=f64(wl["main_k_norm_w"]), eps=spec.eps,
+                slot_mapping=wl["slot_mapping"].cpu().numpy(), kv_dtype=spec.kv_dtype)
+
+
 def kv_scales(spec):
     """(k_scale, v_scale) of the workload's main KV cache (1, 1 for bf16)."""
     return (spec.kv_scale, spec.kv_scale) if spec.kv_dtype == W.DTYPE_E4M3 else (1.0, 1.0)
@@ -38,7 +46,7 @@ def idx_dtype(spec):
 class Step:
     """One GPU layer step of a workload through the C ABI."""
 
-    def __init__(self, wl, gate=True):
+    def __init__(self, wl, gate=True, main=False):
         self.wl = wl
         s = wl.spec
         dev = wl["q"].device
@@ -50,13 +58,15 @@ class Step:
         assert nbytes > 0
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.gate = gate
+        self.main = main  # fuse the main-attention prepare into stage 1
 
     def run(self, skip_topk=False):
         t = dict(self.wl.t)
         if not self.gate:
             t["gate"] = None
-        Q.layer_step(self.cfg, self.gcfg, Q.step_args(t, self.packed, self.out, self.mv), self.ws,
-                     skip_topk=skip_topk)
+        m = Q.main_prep(t, self.wl.spec.eps) if self.main else None
+        Q.layer_step(self.cfg, self.gcfg, Q.step_args(t, self.packed, self.out, self.mv, main=m),
+                     self.ws, skip_topk=skip_topk)
         torch.cuda.synchronize()
         return self
 

@@ -12,7 +12,8 @@ import torch
 from learned_sparse_attention_gb300 import qsa as Q
 from learned_sparse_attention_gb300 import workloads as W
 from oracle import qsa_oracle as O
-from tests.gpu_harness import (Step, cfgs, idx_dtype, max_visible, oracle_gqa_row, random_packed)
+from tests.gpu_harness import (Step, cfgs, idx_dtype, max_visible, oracle_gqa_row, oracle_main,
+                               random_packed)
 from tests.oracle_io import OracleState, f64, i64
 from tests.parity import close_bf16, close_e4m3, selection_ok
 
@@ -559,3 +560,87 @@ def test_mtp_steps_equals_step_by_step_and_oracle():
     sl = sl[sl >= 0]
     ok, err = _close_idx(spec, f64(wa["ccache"]).reshape(-1, 128)[sl], st.ccache.reshape(-1, 128)[sl])
     assert ok, err
+
+
+# ----------------------------------------------------------------- main prepare
+MAIN = {
+    "mid_main_bf16": W.small_spec("mid_main_bf16", seed=30, contexts=(2000, 777, 64),
+                                  rows_per_req=(2, 1, 3), n_heads=16, index_dtype=E4,
+                                  compress_ratio=4, token_topk=256, hq=32, hkv=4, page=64,
+                                  main_prep=True),
+    "mid_main_fp8_mrope_g3": W.small_spec("mid_main_fp8_mrope_g3", seed=31, contexts=(3000, 700),
+                                          rows_per_req=(4, 4), n_heads=8, index_dtype=BF,
+                                          compress_ratio=4, token_topk=128,
+                                          mrope_section=(8, 12, 12), image_span=64, hq=24, hkv=8,
+                                          page=32, kv_dtype=E4, kv_scale=0.05, main_prep=True),
+    "small_main_group16": W.small_spec("small_main_group16", seed=32, hq=32, hkv=2,
+                                       main_prep=True),
+}
+
+
+def _oracle_prepare(spec, wl, st):
+    """The oracle's main-attention prepare over every row: (q, gate) per row,
+    with the rows' K/V written into st.kv (the stored values)."""
+    m = oracle_main(spec, wl)
+    q = np.zeros((spec.rows, spec.hq, 128))
+    gate = np.zeros_like(q)
+    for row in range(spec.rows):
+        q[row], gate[row], k, v = O.prepare_main_row(st.cfg, m["qkv"][row], st.positions[row],
+                                                     st.cos_sin, m["q_norm_w"], m["k_norm_w"],
+                                                     m["eps"], spec.hq, spec.hkv)
+        O.write_main_kv(st.kv, int(m["slot_mapping"][row]), k, v, spec.page, spec.kv_dtype,
+                        *st.kv_scales)
+    return q, gate
+
+
+def _kv_rows_close(spec, got_kv, want_kv, slots):
+    D = 128
+    for slot in slots:
+        blk, off = slot // spec.page, slot % spec.page
+        g, w = got_kv[blk, :, off], want_kv[blk, :, off]
+        if spec.kv_dtype == E4:
+            ok, err = close_e4m3(g, w)
+        else:
+            ok, err = close_bf16(g[:, :D], w[:, :D])
+            ok = ok and np.array_equal(g[:, D:], w[:, D:])  # v is copied
+        assert ok, f"KV row of slot {slot}: {err}"
+
+
+@pytest.mark.parametrize("name", list(MAIN))
+def test_main_prepare_matches_oracle(name):
+    """qsa_main_prepare alone: q (bf16), the gate (copied) and the rows' K/V
+    in the cache (bf16 or e4m3), the rest of the cache untouched."""
+    spec = MAIN[name]
+    wl = W.make_workload(spec, device="cuda")
+    st = OracleState(wl)
+    cfg, gcfg = cfgs(spec, wl)
+    Q.main_prepare(cfg, gcfg, Q.main_prep(wl.t, spec.eps), wl["positions"], wl["cos_sin"])
+    torch.cuda.synchronize()
+    assert Q.check_errors() == 0
+    q, gate = _oracle_prepare(spec, wl, st)
+    ok, err = close_bf16(f64(wl["main_q_out"]), q)
+    assert ok, f"q: {err}"
+    np.testing.assert_array_equal(f64(wl["main_gate_out"]), gate)
+    got_kv = f64(wl["kv"])
+    slots = wl["slot_mapping"].cpu().numpy()
+    _kv_rows_close(spec, got_kv, st.kv, slots)
+    mask = np.ones(got_kv.shape[:3], dtype=bool)
+    for slot in slots:
+        mask[slot // spec.page, :, slot % spec.page] = False
+    np.testing.assert_array_equal(got_kv[mask], st.kv[mask])
+
+
+@pytest.mark.parametrize("name", list(MAIN))
+def test_layer_step_with_fused_main_prepare(name):
+    """The layer step with the main-attention prepare fused into stage 1:
+    stage 4 attends with the prepared q and gate over the cache that holds
+    this step's own K/V rows (selected as the newest tokens)."""
+    spec = MAIN[name]
+    wl = W.make_workload(spec, device="cuda")
+    st = OracleState(wl)
+    step = Step(wl, main=True).run()
+    assert Q.check_errors() == 0
+    st.compress()
+    st.q, st.gate = _oracle_prepare(spec, wl, st)
+    _full_chain(spec, wl, st, step)
+    _kv_rows_close(spec, f64(wl["kv"]), st.kv, wl["slot_mapping"].cpu().numpy())
