@@ -316,6 +316,9 @@ def algorithmic_bytes(spec, wl, packed):
     groups = int((wl["compressed_slots"] >= 0).sum().item())
     stage1 = rows * (spec.n_heads * D * 2 + 2 * D * 2 + spec.n_heads * D * e_idx) + groups * (
         (r - 1) * D * 2 + D * e_idx)
+    if spec.main_prep:  # projection rows in; q, gate and the rows' K/V out
+        stage1 += rows * ((2 * spec.hq + 2 * spec.hkv) * D * 2 + 2 * spec.hq * D * 2
+                          + spec.hkv * 2 * D * e_kv)
     main_io = rows * 3 * spec.hq * D * 2
     packed_io = rows * 2 * 4 * spec.packed_width
     step = keys + kv + stage1 + main_io + packed_io

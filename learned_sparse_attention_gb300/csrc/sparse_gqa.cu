@@ -257,24 +257,24 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   const float sl2 = 0.08838834764831845f * kLog2e * (KVT ? P.k_scale : 1.0f);
   bool bad = false;
 
-  // KV row ids of the selected tokens tok[u] (u < NB) into
+  // KV row ids of the selected tokens tok[u] (u < NT) into
   // s_rowid[i0 + u * kThreads]; entries at or past cn are not touched.
   // (pages are a power of two in practice: shift and mask instead of a
   // division there)
   const bool page_pow2 = (P.page & (P.page - 1)) == 0;
   const int page_shift = __ffs(P.page) - 1;
   auto resolve = [&](auto& tok, int i0, int cn) {
-    constexpr int NB = sizeof(tok) / sizeof(tok[0]);
-    int pid[NB], off[NB];
+    constexpr int NT = sizeof(tok) / sizeof(tok[0]);
+    int pid[NT], off[NT];
 #pragma unroll
-    for (int u = 0; u < NB; ++u) {
+    for (int u = 0; u < NT; ++u) {
       const int blk = tok[u] < 0 ? -1 : page_pow2 ? tok[u] >> page_shift : tok[u] / P.page;
       off[u] = tok[u] - blk * P.page;
       pid[u] = -1;
       if (tok[u] >= 0 && blk < P.bt_stride) pid[u] = sbt ? s_bt[blk] : bt_row[blk];
     }
 #pragma unroll
-    for (int u = 0; u < NB; ++u) {
+    for (int u = 0; u < NT; ++u) {
       const int i = i0 + u * kThreads;
       if (i >= cn) continue;
       const uint32_t rid = kv_row_id(P, off[u], pid[u], kvh);
