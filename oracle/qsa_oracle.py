@@ -414,6 +414,25 @@ def write_main_kv(kv, slot: int, k, v, page: int, kv_dtype: int = DTYPE_BF16,
         kv[blk, :, off, D:] = round_bf16(v)
 
 
+def qkv_index_projection(x, w, qkv_cols: int, index_q_cols: int):
+    """The fused projection of the main attention and the indexer: one GEMM
+    y = x . w^T over the stacked weights [w_qkv; w_index_q; w_index_k], the
+    output rounded once to bf16 and split into (main qkv rows, the indexer's
+    projected_q, its raw keys).
+
+    Follows "vllm.models.qwen4_exp.nvidia.qsa": Qwen4ExpQSAQKVIndexerLinear
+    ("Pack sharded Q/gate, K, V and replicated indexer Q/K in one GEMM",
+    the indexer's weights as shard 3), Qwen4ExpQSAAttention.forward (qkv,
+    projected_qk = qkv.split([2 * q_size + 2 * kv_size, index_qk_size])) and
+    QSAIndexer.forward (projected_q, raw_keys = projected_qk.split(
+    (index_n_heads * D, index_kv_heads * D))).  x: [rows, hidden]; w:
+    [qkv_cols + index_q_cols + D_k, hidden] (values).
+    """
+    y = round_bf16(np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T)
+    return (y[:, :qkv_cols], y[:, qkv_cols:qkv_cols + index_q_cols],
+            y[:, qkv_cols + index_q_cols:])
+
+
 # ---------------------------------------------------------------------------
 # Stage 2: index logits; stage 3: block top-k and expand
 # ---------------------------------------------------------------------------

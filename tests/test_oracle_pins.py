@@ -664,3 +664,39 @@ def test_write_main_kv_slot_and_dtypes():
     before = kv8.copy()
     O.write_main_kv(kv8, -1, k, v, 16)
     np.testing.assert_array_equal(kv8, before)
+
+
+# --------------------------------------------------------------------------
+# Fused qkv + indexer projection
+# --------------------------------------------------------------------------
+
+def test_projection_exact_on_small_integers():
+    """Small-integer inputs make every product and sum exact (and exactly a
+    bf16 value): the oracle must equal plain integer arithmetic, done here
+    with Python ints."""
+    rng = np.random.default_rng(5)
+    rows, hidden, qc, iq = 3, 48, 8, 6
+    x = rng.integers(-3, 4, size=(rows, hidden))
+    w = rng.integers(-3, 4, size=(qc + iq + 4, hidden))
+    qkv, pq, rk = O.qkv_index_projection(x.astype(float), w.astype(float), qc, iq)
+    full = [[sum(int(x[i, k]) * int(w[j, k]) for k in range(hidden)) for j in range(w.shape[0])]
+            for i in range(rows)]
+    full = np.array(full, dtype=np.float64)
+    np.testing.assert_array_equal(qkv, full[:, :qc])
+    np.testing.assert_array_equal(pq, full[:, qc:qc + iq])
+    np.testing.assert_array_equal(rk, full[:, qc + iq:])
+
+
+def test_projection_routes_columns_by_the_stacked_weights():
+    """A one-hot input row k returns column k of the stacked weights; rows of
+    the three weight blocks hold distinct constants, so each output lands in
+    its own buffer (main qkv, then indexer q, then the indexer key)."""
+    hidden, qc, iq, dk = 16, 5, 3, 2
+    w = np.concatenate([np.full((qc, hidden), 1.0), np.full((iq, hidden), 2.0),
+                        np.full((dk, hidden), 3.0)]) * (1 + np.arange(hidden))[None, :]
+    x = np.eye(hidden)[[0, 7, 15]]
+    qkv, pq, rk = O.qkv_index_projection(x, w, qc, iq)
+    for i, k in enumerate([0, 7, 15]):
+        np.testing.assert_array_equal(qkv[i], np.full(qc, 1.0 * (k + 1)))
+        np.testing.assert_array_equal(pq[i], np.full(iq, 2.0 * (k + 1)))
+        np.testing.assert_array_equal(rk[i], np.full(dk, 3.0 * (k + 1)))
