@@ -552,6 +552,38 @@ def mtp_report(device, steps, warmup, flush, drain, hbm):
     return res
 
 
+def projection_report(device, steps, flush, drain, bf16, hbm, hidden=4096):
+    """The fused qkv + indexer projection GEMM of a 32q/4kv x 128 layer with
+    a 32-head indexer over hidden = 4096 (synthetic weights; the pages do not
+    give hidden_size), at the decode batch's 64 rows (bound by reading the
+    weights) and the prefill chunk's 16384 rows (bound by the tensor cores)."""
+    qc, iq, ik = (2 * 32 + 2 * 4) * 128, 32 * 128, 128
+    ncols = qc + iq + ik
+    g = torch.Generator(device=device).manual_seed(11)
+    w = (torch.randn((ncols, hidden), generator=g, device=device) / hidden ** 0.5).to(torch.bfloat16)
+    res = {"hidden": hidden, "columns": {"qkv": qc, "index_q": iq, "index_k": ik},
+           "weights": "synthetic N(0, 1/hidden)"}
+    for name, rows in (("decode_batch", 64), ("chunked_prefill", 16384)):
+        x = torch.randn((rows, hidden), generator=g, device=device).to(torch.bfloat16)
+        outs = [torch.empty((rows, c), dtype=torch.bfloat16, device=device) for c in (qc, iq, ik)]
+        fn = lambda: Q.qkv_index_proj(x, w, *outs)
+        fn()
+        torch.cuda.synchronize()
+        ms = statistics.median(timed(fn, steps, flush, drain))
+        flops = 2.0 * rows * hidden * ncols
+        nbytes = (ncols * hidden + rows * hidden + rows * ncols) * 2
+        tf = flops / (ms / 1000.0) / 1e12
+        gbs = nbytes / (ms / 1000.0) / 1e9
+        res[name] = {"rows": rows, "ms": ms, "tflops": tf, "frac_bf16": tf / bf16,
+                     "gbs": gbs, "frac_hbm": gbs / hbm, "flops": flops, "bytes": nbytes}
+        del x, outs
+    if Q.check_errors() != 0:
+        raise RuntimeError("device error word set during the projection measurement")
+    del w
+    torch.cuda.empty_cache()
+    return res
+
+
 def prefill_report(device, steps, flush, drain, fp8, bf16, cpu_baseline):
     """The chunked-prefill workload (one request, 16384 new rows after a
     32768-token prefix): layer-step rows/s; the index-logits kernel alone
@@ -700,7 +732,8 @@ def run_ours(args):
                                                      drain, hbm),
                  "decode_batch_prepare": decode_report("decode_batch_prepare", device, 10, 3,
                                                        flush, drain, hbm),
-                 "mtp_mrope": mtp_report(device, 10, 3, flush, drain, hbm)}
+                 "mtp_mrope": mtp_report(device, 10, 3, flush, drain, hbm),
+                 "qkv_index_projection": projection_report(device, 5, flush, drain, bf16, hbm)}
 
     if rank == 0:
         line = {

@@ -282,6 +282,30 @@ qsa_status qsa_main_prepare(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const q
                             const int64_t* positions, const float* cos_sin, int32_t rows,
                             void* stream);
 
+/*
+ * qsa_qkv_index_proj -- the fused projection that feeds the layer step: one
+ * GEMM y = x . w^T (bf16 inputs, fp32 accumulation on the tensor cores, one
+ * bf16 rounding) over the stacked weights of the main attention and the
+ * indexer, written as three row-major outputs.  Follows
+ * "vllm.models.qwen4_exp.nvidia.qsa", Qwen4ExpQSAQKVIndexerLinear (the
+ * indexer's index_qk_proj packed as shard 3 of the qkv GEMM),
+ * Qwen4ExpQSAAttention.forward (qkv, projected_qk = qkv.split([2 q_size +
+ * 2 kv_size, index_qk_size])) and QSAIndexer.forward (projected_q, raw_keys
+ * = projected_qk.split((index_n_heads D, index_kv_heads D))).
+ *  x            [rows, hidden] bf16, 16-byte aligned; hidden a multiple of 64
+ *  w            [qkv_cols + index_q_cols + index_k_cols, hidden] bf16, 16-byte
+ *               aligned: the main qkv weights (per query head [q | gate],
+ *               then K, then V heads), then the indexer's query heads, then
+ *               its key head
+ *  qkv_out      [rows, qkv_cols] bf16 (the layer step's main qkv rows)
+ *  index_q_out  [rows, index_q_cols] bf16 (projected_q)
+ *  index_k_out  [rows, index_k_cols] bf16 (raw_keys)
+ * An output may be NULL when its column count is 0.
+ */
+qsa_status qsa_qkv_index_proj(const void* x, const void* w, int32_t rows, int32_t hidden,
+                              int32_t qkv_cols, int32_t index_q_cols, int32_t index_k_cols,
+                              void* qkv_out, void* index_q_out, void* index_k_out, void* stream);
+
 /* Arguments of one fused layer step (all device pointers; meanings as in the
  * stage calls above). */
 typedef struct qsa_step_args {

@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libqsa.so")
 
 SOURCES = ["abi.cu", "compress.cu", "index_logits.cu", "topk.cu", "sparse_gqa.cu",
-           "sparse_gqa_noalloc.cu"]
+           "sparse_gqa_noalloc.cu", "proj_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

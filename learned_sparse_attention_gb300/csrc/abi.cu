@@ -75,6 +75,21 @@ struct ValidateOnly {
   ~ValidateOnly() { t_validate_only = false; }
 };
 
+// 2-D bf16 map over [outer, inner] row-major with a box of 64 elements x
+// box_rows rows, 128-byte swizzle, zero fill out of bounds.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, long long inner, long long outer,
+                    int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * 2)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -629,6 +644,41 @@ qsa_status qsa_layer_step(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa
   return do_gqa(gcfg, q4, a->kv, a->block_table, a->bt_stride, a->packed, pw, a->token_to_req,
                 gate4, a->out, a->rows, w + L.gqa_ws, L.total - L.gqa_ws, s, /*pdl=*/true,
                 /*tickets_zeroed=*/tickets != nullptr, /*q_after_wait=*/mp != nullptr);
+}
+
+qsa_status qsa_qkv_index_proj(const void* x, const void* w, int32_t rows, int32_t hidden,
+                              int32_t qkv_cols, int32_t index_q_cols, int32_t index_k_cols,
+                              void* qkv_out, void* index_q_out, void* index_k_out, void* stream) {
+  if (rows < 0 || hidden < 0 || qkv_cols < 0 || index_q_cols < 0 || index_k_cols < 0)
+    return QSA_ERR_SHAPE;
+  if (rows == 0) return QSA_OK;
+  if (hidden < 64 || hidden % 64 != 0) return QSA_ERR_SHAPE;
+  const long long ncols = static_cast<long long>(qkv_cols) + index_q_cols + index_k_cols;
+  if (ncols < 1 || ncols >= (1ll << 31)) return QSA_ERR_SHAPE;
+  if (!x || !w || (qkv_cols && !qkv_out) || (index_q_cols && !index_q_out) ||
+      (index_k_cols && !index_k_out))
+    return QSA_ERR_INVALID_ARG;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w);
+  const uintptr_t a2 = reinterpret_cast<uintptr_t>(qkv_out) | reinterpret_cast<uintptr_t>(index_q_out) |
+                       reinterpret_cast<uintptr_t>(index_k_out);
+  if ((a16 & 15) || (a2 & 1)) return QSA_ERR_INVALID_ARG;
+  ProjParams p{};
+  p.qkv_out = static_cast<uint16_t*>(qkv_out);
+  p.index_q_out = static_cast<uint16_t*>(index_q_out);
+  p.index_k_out = static_cast<uint16_t*>(index_k_out);
+  p.rows = rows;
+  p.hidden = hidden;
+  p.ncols = static_cast<int>(ncols);
+  p.qkv_cols = qkv_cols;
+  p.index_q_cols = index_q_cols;
+  p.index_k_cols = index_k_cols;
+  p.err = error_word();
+  if (p.err == nullptr) return QSA_ERR_CUDA;
+  CUtensorMap tw, tx;
+  if (!encode_bf16_2d(&tw, w, hidden, ncols, 128) ||
+      !encode_bf16_2d(&tx, x, hidden, rows, proj_tile_rows(rows)))
+    return QSA_ERR_CUDA;
+  return cuda_status(launch_proj_gemm(p, tw, tx, static_cast<cudaStream_t>(stream)));
 }
 
 qsa_status qsa_main_prepare(const qsa_cfg* cfg, const qsa_gqa_cfg* gcfg, const qsa_main_prep* m,

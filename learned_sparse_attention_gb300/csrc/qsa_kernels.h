@@ -126,4 +126,20 @@ int gqa_num_splits(int rows, int hkv, int packed_width, int sms);
 cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
                               bool zero_tickets = true);
 
+// The fused projection GEMM: y = x . w^T (bf16 in, fp32 accumulate, bf16
+// out), output columns routed to the main qkv rows, then the indexer's query
+// and key rows.
+struct ProjParams {
+  uint16_t* qkv_out;      // [rows, qkv_cols]
+  uint16_t* index_q_out;  // [rows, index_q_cols]
+  uint16_t* index_k_out;  // [rows, index_k_cols]
+  int rows, hidden, ncols, qkv_cols, index_q_cols, index_k_cols;
+  unsigned long long* err;
+};
+int proj_tile_rows(int rows);  // input rows per CTA tile (64, 128 or 256)
+// tmap_w: [ncols, hidden] bf16, box 64 x 128 rows; tmap_x: [rows, hidden]
+// bf16, box 64 x proj_tile_rows(rows) rows; both 128-byte swizzled.
+cudaError_t launch_proj_gemm(const ProjParams& p, const CUtensorMap& tmap_w,
+                             const CUtensorMap& tmap_x, cudaStream_t stream);
+
 }  // namespace qsa

@@ -88,6 +88,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qsa_layer_step": [P, P, P, I, P, Z, P],
         "qsa_mtp_steps": [P, P, P, I, P, Z, P],
         "qsa_main_prepare": [P, P, P, P, P, I, P],
+        "qsa_qkv_index_proj": [P, P, I, I, I, I, I, P, P, P, P],
         "qsa_workspace_bytes": [P, P, I, I, I],
         "qsa_status_string": [I],
         "qsa_check_errors": [ctypes.POINTER(ctypes.c_int64)],
@@ -312,6 +313,18 @@ def mtp_steps(cfg, gcfg, steps, ws, stream=None):
     st = load().qsa_mtp_steps(ctypes.byref(cfg), ctypes.byref(gcfg), arr, k, _ptr(ws, torch.uint8),
                               ws.numel(), _stream(stream))
     _check("qsa_mtp_steps", st)
+
+
+def qkv_index_proj(x, w, qkv_out, index_q_out, index_k_out, stream=None):
+    """The fused projection GEMM (qsa_qkv_index_proj): x [rows, hidden] .
+    w^T with w = [w_qkv; w_index_q; w_index_k], into the three outputs."""
+    rows, hidden = x.shape
+    st = load().qsa_qkv_index_proj(
+        _ptr(x, torch.bfloat16, "x"), _ptr(w, torch.bfloat16, "w"), rows, hidden,
+        qkv_out.shape[-1], index_q_out.shape[-1], index_k_out.shape[-1],
+        _ptr(qkv_out, torch.bfloat16), _ptr(index_q_out, torch.bfloat16),
+        _ptr(index_k_out, torch.bfloat16), _stream(stream))
+    _check("qsa_qkv_index_proj", st)
 
 
 def step_launches(cfg, gcfg, rows, reqs, skip_topk=False) -> int:
