@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("rows,hidden,qc,iq,ik", [
     (5, 64, 100, 60, 28),          # ragged everything, one K slice
     (64, 512, 1152, 512, 128),     # decode-sized tile, 8 K slices
+    (40, 960, 300, 200, 28),       # 15 K slices, ragged columns in every buffer
     (300, 1024, 640, 256, 128),    # two N tiles of 256 rows, a ragged one
     (64, 4096, 9216, 4096, 128),   # decode batch of the layer
     (2048, 4096, 9216, 4096, 128), # a prefill slice of the layer
