@@ -449,6 +449,7 @@ qsa_status do_gqa(const qsa_gqa_cfg* gcfg, const void* q, const void* kv,
   p.num_blocks = gcfg->num_blocks;
   const GqaLayout G = gqa_layout(gcfg, rows, packed_width);
   p.splits = G.splits;
+  p.sms = sm_count();
   if (G.total > 0) {
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255)) return QSA_ERR_WORKSPACE;
     if (ws_bytes < G.total) return QSA_ERR_WORKSPACE;

@@ -117,6 +117,7 @@ struct GqaParams {
   int kv_dtype;            // 0: bf16, 1: e4m3 with static scales
   float k_scale, v_scale;  // e4m3: stored value * scale = cached value
   int q_after_wait;        // q and gate are written by the kernels before this one
+  int sms;                 // multiprocessors of the device (launch shape)
   unsigned long long* err;
 };
 // Split-KV factor for `rows` rows on a device with `sms` multiprocessors.

@@ -49,15 +49,18 @@ constexpr int kMaxTiles = 40;                // tiles of one row-id chunk
 constexpr int kMaxTok = kMaxTiles * kTile;   // token row ids staged at a time
 constexpr uint32_t kBadRow = 0xFFFFFFFFu;
 
-// Shared-memory plan per KV dtype (KVT 0: bf16, 1: e4m3).  A warp's stage
-// holds its 16 tokens' K rows, then their V rows, in 16-byte chunks
-// XOR-swizzled by token.  e4m3 rows are half as wide, so the ring is deeper
-// at the same footprint, and each warp has an f16 tile it decodes V into
-// (a 3-stage e4m3 ring at three CTAs per SM measured the same).
-template <int KVT>
+// Shared-memory plan per KV dtype (KVT 0: bf16, 1: e4m3) and ring depth
+// ST.  A warp's stage holds its 16 tokens' K rows, then their V rows, in
+// 16-byte chunks XOR-swizzled by token.  e4m3 rows are half as wide, so the
+// ring is deeper at the same footprint, and each warp has an f16 tile it
+// decodes V into (a 3-stage e4m3 ring at three CTAs per SM measured the
+// same).  bf16 runs 3 stages at two CTAs per SM when the launch is about
+// one wave (HBM latency to hide), 2 stages at three CTAs per SM when it is
+// many waves (prefill: K/V mostly from L2, and more warps to issue).
+template <int KVT, int ST>
 struct KvPlan {
   static constexpr int kRowB = KVT ? 256 : 512;          // K|V bytes of one (token, KV head)
-  static constexpr int kStages = KVT ? 5 : 3;
+  static constexpr int kStages = ST;
   static constexpr int kSlab = 16 * kRowB;                // bytes per warp stage
   static constexpr int kPipe = kWarps * kStages * kSlab;
   static constexpr int kVf16 = KVT ? kWarps * 16 * 256 : 0;  // per-warp f16 V tiles
@@ -125,9 +128,9 @@ __device__ __forceinline__ uint32_t kv_row_id(const GqaParams& P, int off, int p
 // NB: column blocks of 8 query heads (1 for groups of 1-8, 2 for 16).
 // KVT: KV cache dtype, 0 bf16, 1 e4m3 with static scales (f16 MMAs: every
 // e4m3 value and every bf16 query of normal range is exact in f16).
-template <int NB, int KVT>
+template <int NB, int KVT, int ST>
 __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
-  using KP = KvPlan<KVT>;
+  using KP = KvPlan<KVT, ST>;
   constexpr int kStages = KP::kStages;
   constexpr int kSlab = KP::kSlab;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -606,21 +609,25 @@ cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
     return cudaErrorInvalidValue;
   if (p.group < 1 || (p.group > 8 && p.group != 16)) return cudaErrorInvalidValue;
   if (p.kv_dtype != 0 && p.kv_dtype != 1) return cudaErrorInvalidValue;
-  void (*kerns[2][2])(const GqaParams) = {{gqa_kernel<1, 0>, gqa_kernel<1, 1>},
-                                          {gqa_kernel<2, 0>, gqa_kernel<2, 1>}};
-  const int smems[2] = {KvPlan<0>::kSmem, KvPlan<1>::kSmem};
+  // kernels by [column blocks][ring plan: bf16 3 stages, bf16 2 stages, e4m3 5 stages]
+  void (*kerns[2][3])(const GqaParams) = {
+      {gqa_kernel<1, 0, 3>, gqa_kernel<1, 0, 2>, gqa_kernel<1, 1, 5>},
+      {gqa_kernel<2, 0, 3>, gqa_kernel<2, 0, 2>, gqa_kernel<2, 1, 5>}};
+  const int smems[3] = {KvPlan<0, 3>::kSmem, KvPlan<0, 2>::kSmem, KvPlan<1, 5>::kSmem};
   const int ki = p.group <= 8 ? 0 : 1;
-  auto kern = kerns[ki][p.kv_dtype];
-  const int kSmem = smems[p.kv_dtype];
-  static bool attr_set[2][2][64] = {};
+  const long long ctas = static_cast<long long>(p.rows) * p.hkv * p.splits;
+  const int plan = p.kv_dtype == 1 ? 2 : (ctas > 4ll * (p.sms > 0 ? p.sms : 1) ? 1 : 0);
+  auto kern = kerns[ki][plan];
+  const int kSmem = smems[plan];
+  static bool attr_set[2][3][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[ki][p.kv_dtype][dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[ki][plan][dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[ki][p.kv_dtype][dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[ki][plan][dev] = true;
   }
   if (p.splits > 1 && p.counters != nullptr && zero_tickets) {
     cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(unsigned) * p.rows * p.hkv, stream);

@@ -99,6 +99,7 @@ extern "C" qsa_status qsa_sparse_gqa_noalloc(const qsa_gqa_cfg* gcfg, const void
   p.page = gcfg->page_size;
   p.num_blocks = gcfg->num_blocks;
   p.splits = qsa::gqa_num_splits(rows, gcfg->num_kv_heads, packed_width, qsa::sm_count());
+  p.sms = qsa::sm_count();
   if (p.splits > 1) {
     const size_t po = static_cast<size_t>(p.splits) * rows * p.hq * 128 * sizeof(float);
     const size_t pl = static_cast<size_t>(p.splits) * rows * p.hq * sizeof(float);

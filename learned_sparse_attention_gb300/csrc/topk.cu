@@ -295,13 +295,15 @@ __device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
 // KPT: keys per thread the loops are unrolled for (4, 8, 16 or 32), the
 // smallest that covers the launch's max_visible with CL * NT threads.
 // NT: 512, or 1024 when there are fewer rows than half the SMs.
-// CL: CTAs per row, one thread-block cluster (1 or 2).  With CL > 1
+// CL: CTAs per row, one thread-block cluster (1, 2 or 4).  With CL > 1
 // the row's blocks are split in order over the cluster's CTAs; each radix
 // pass sums the CTAs' shared histograms through distributed shared memory,
 // so every CTA reaches the same digit, and one exchange of per-CTA counts
-// places each CTA's selected blocks in the packed row.
+// places each CTA's selected blocks in the packed row.  A CTA lists its
+// selected blocks in shared memory first and then expands them into their
+// r tokens each with coalesced stores.
 template <int KPT, int NT, int CL>
-__global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const TopkParams P) {
+__global__ void __launch_bounds__(NT, NT == 512 && CL <= 2 ? 2 : 1) topk_reg_kernel(const TopkParams P) {
   namespace cg = cooperative_groups;
   constexpr int NW = NT / 32;
   constexpr int GT = CL * NT;  // threads per row
@@ -313,6 +315,8 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
   __shared__ int s_digit, s_k, s_cnt, s_ncand;
   __shared__ uint32_t s_cmm[2];  // this CTA's (min, max) key, read by the cluster
   __shared__ int s_ccnt[2];      // this CTA's (greater, equal) counts, read by the cluster
+  constexpr int kSelCap = KPT * NT < kRegKeys * kRegThreads / 4 ? KPT * NT : kRegKeys * kRegThreads / 4;
+  __shared__ int s_sel[kSelCap];  // this CTA's selected blocks in block order
 
   griddep_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -437,6 +441,8 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
       const int width = hi + 1 < kDigitBits ? hi + 1 : kDigitBits;
       const int shift = hi - width + 1;
       const uint32_t dmask = (1u << width) - 1u;
+      // (warp-aggregated variants -- match.any groups, or one add for a
+      // warp whose keys share a bin -- measured slower or equal)
 #pragma unroll
       for (int j = 0; j < KPT; ++j)
         if (key[j] != 0u && (key[j] & pmask) == prefix) atomicAdd(&hist[(key[j] >> shift) & dmask], 1);
@@ -549,8 +555,8 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
     int tot;
     const int both = block_sum_excl<NW>((__popc(gt_mask) << 16) | __popc(eq_mask), scratch, &tot);
     int gt_before = both >> 16, eq_before = both & 0xFFFF;
+    int cta_gt = 0, cta_eq = 0;  // counts of the CTAs holding lower blocks
     if constexpr (CL > 1) {
-      // counts of the CTAs holding lower blocks
       if (tid == 0) {
         s_ccnt[0] = tot >> 16;
         s_ccnt[1] = tot & 0xFFFF;
@@ -559,23 +565,36 @@ __global__ void __launch_bounds__(NT, NT == 512 ? 2 : 1) topk_reg_kernel(const T
       cluster.sync();
       for (int c = 0; c < crank; ++c) {
         const int* o = cluster.map_shared_rank(s_ccnt, c);
-        gt_before += o[0];
-        eq_before += o[1];
+        cta_gt += o[0];
+        cta_eq += o[1];
       }
+      gt_before += cta_gt;
+      eq_before += cta_eq;
     }
     int take = keq - eq_before;
     take = take < 0 ? 0 : take;
     uint32_t eq_take = eq_mask;
     for (int c = __popc(eq_mask); c > take; --c) eq_take &= ~(1u << (31 - __clz(eq_take)));
     uint32_t m = gt_mask | eq_take;
-    int out = gt_before + (eq_before < keq ? eq_before : keq);
+    // this CTA's selected blocks occupy packed slots [out0, out0 + nloc)
+    int out0 = 0, nloc = nsel;
+    if constexpr (CL > 1) {
+      out0 = cta_gt + (cta_eq < keq ? cta_eq : keq);
+      int eq_loc = keq - cta_eq;
+      eq_loc = eq_loc < 0 ? 0 : eq_loc > (tot & 0xFFFF) ? (tot & 0xFFFF) : eq_loc;
+      nloc = (tot >> 16) + eq_loc;
+    }
+    int out = gt_before + (eq_before < keq ? eq_before : keq) - out0;
     while (m) {
-      const int j = __ffs(m) - 1;
-      const int b = base + j;
-      int32_t* dst = prow + out * r;
-      for (int t = 0; t < r; ++t) dst[t] = b * r + t;
-      ++out;
+      s_sel[out++] = base + __ffs(m) - 1;
       m &= m - 1u;
+    }
+    __syncthreads();
+    // block b -> tokens b r .. b r + r - 1, consecutive slots of the packed row
+    int32_t* dst = prow + out0 * r;
+    for (int idx = tid; idx < nloc * r; idx += NT) {
+      const int i = idx / r;
+      dst[idx] = s_sel[i] * r + (idx - i * r);
     }
     // the tail tokens of the open group, then -1 padding
     for (int idx = nsel * r + gtid; idx < W; idx += GT)
@@ -599,28 +618,50 @@ size_t topk_smem_bytes(int max_visible, int block_topk) {
   return static_cast<size_t>(max_visible) * 4 + static_cast<size_t>(block_topk) * 4 + 16;
 }
 
+namespace {
+
+// One cluster of CL 512-thread CTAs per row, keys per thread for max_visible.
+template <int CL>
+cudaError_t launch_topk_cluster(const TopkParams& p, cudaStream_t stream, bool pdl) {
+  const int kpt = (p.max_visible + CL * kRegThreads - 1) / (CL * kRegThreads);
+  const dim3 g(p.rows * CL), b(kRegThreads);
+  if (kpt <= 4) return launch_kernel_cluster(topk_reg_kernel<4, kRegThreads, CL>, g, b, 0, stream, pdl, CL, p);
+  if (kpt <= 8) return launch_kernel_cluster(topk_reg_kernel<8, kRegThreads, CL>, g, b, 0, stream, pdl, CL, p);
+  return launch_kernel_cluster(topk_reg_kernel<16, kRegThreads, CL>, g, b, 0, stream, pdl, CL, p);
+}
+
+// CTAs per row for rows of more than 4096 keys: 0 = one 1024-thread CTA,
+// else a cluster of that many 512-thread CTAs.  Measured on GB300: many
+// rows gain from pairs while the pairs fit one wave at two CTAs per SM; a
+// few rows of many keys (long-context decode, 8 rows of 16 384 keys) gain
+// ~1 us from four CTAs per row on four SMs; 2 or 8 CTAs per row, and
+// clusters for a decode batch of 64 rows, were slower than one 1024-thread
+// CTA per row.
+int topk_cluster_size(int rows, int max_visible, int sms) {
+  const long long s = sms > 0 ? sms : 1;
+  if (rows >= 76) return 2LL * rows <= 2 * s ? 2 : 1;
+  if (4LL * rows <= s && max_visible > 8 * 1024) return 4;
+  return 0;
+}
+
+}  // namespace
+
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
   if (p.max_visible <= kRegKeys * kRegThreads && p.token_topk / p.ratio <= kRegKeys * kRegThreads / 4) {
     const dim3 b(kRegThreads);
-    // Many rows with long key lists: a cluster of two 512-thread CTAs per
-    // row (half the keys per thread) while the rows' CTAs still fit one wave
-    // at two per SM.  Measured: fewer rows gain nothing from clusters over
-    // one 1024-thread CTA per row (below), and larger clusters cost more in
-    // cluster barriers than they save.
-    const long long slots = 2LL * (p.sms > 0 ? p.sms : 1);
-    if (p.rows >= 76 && 2LL * p.rows <= slots && p.max_visible > 4 * 1024) {
-      const int kpt = (p.max_visible + 2 * kRegThreads - 1) / (2 * kRegThreads);
-      const dim3 g(p.rows * 2);
-      if (kpt <= 4) return launch_kernel_cluster(topk_reg_kernel<4, kRegThreads, 2>, g, b, 0, stream, pdl, 2, p);
-      if (kpt <= 8) return launch_kernel_cluster(topk_reg_kernel<8, kRegThreads, 2>, g, b, 0, stream, pdl, 2, p);
-      return launch_kernel_cluster(topk_reg_kernel<16, kRegThreads, 2>, g, b, 0, stream, pdl, 2, p);
-    }
-    // few rows, short keys: twice the threads per row, half the keys per thread
-    if (p.rows < 76 && p.max_visible > 4 * 1024) {
-      const int kpt = (p.max_visible + 1023) / 1024;
-      if (kpt <= 8) return launch_kernel(topk_reg_kernel<8, 1024, 1>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
-      return launch_kernel(topk_reg_kernel<16, 1024, 1>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
+    if (p.max_visible > 4 * 1024) {
+      switch (topk_cluster_size(p.rows, p.max_visible, p.sms)) {
+        case 4: return launch_topk_cluster<4>(p, stream, pdl);
+        case 2: return launch_topk_cluster<2>(p, stream, pdl);
+        case 0: {
+          // one 1024-thread CTA per row, half the keys per thread
+          const int kpt = (p.max_visible + 1023) / 1024;
+          if (kpt <= 8) return launch_kernel(topk_reg_kernel<8, 1024, 1>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
+          return launch_kernel(topk_reg_kernel<16, 1024, 1>, dim3(p.rows), dim3(1024), 0, stream, pdl, p);
+        }
+        default: break;
+      }
     }
     const int kpt = (p.max_visible + kRegThreads - 1) / kRegThreads;
     const dim3 g(p.rows);

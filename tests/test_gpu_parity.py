@@ -290,6 +290,43 @@ def test_split_kv_invariance():
         assert ok, err
 
 
+def test_ring_plans_agree():
+    """Stage 4 runs a 3-stage ring at two CTAs per SM for launches of about
+    one wave and a 2-stage ring at three CTAs per SM for many waves; the
+    arithmetic is the same, so rows computed in a many-wave launch equal the
+    same rows computed in a small launch bit for bit."""
+    rows = 720
+    spec = W.small_spec("plans", seed=31, contexts=[2500] * rows, rows_per_req=[1] * rows,
+                        n_heads=8, index_dtype=BF, compress_ratio=4, token_topk=256,
+                        hq=32, hkv=4, page=64)
+    wl = W.make_workload(spec, device="cuda")
+    _, gcfg = cfgs(spec, wl)
+    assert Q.gqa_splits(gcfg, rows, spec.packed_width) == 1
+    st = OracleState(wl, with_kv=False)
+    rng = np.random.default_rng(9)
+    packed = torch.from_numpy(random_packed(rng, st.cfg, st.logical_positions,
+                                            full_rows=set(range(0, rows, 3)))).cuda()
+    ws = torch.empty(1 << 26, dtype=torch.uint8, device="cuda")
+    out_all = torch.empty_like(wl["q"])
+    Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], packed, wl["token_to_req"],
+                 wl["gate"], out_all, ws)
+    few = 60  # 240 CTAs: the one-wave plan
+    assert Q.gqa_splits(gcfg, few, spec.packed_width) == 1
+    out_few = torch.empty_like(wl["q"][:few])
+    Q.sparse_gqa(gcfg, wl["q"][:few].contiguous(), wl["kv"], wl["block_table"],
+                 packed[:few].contiguous(), wl["token_to_req"][:few].contiguous(),
+                 wl["gate"][:few].contiguous(), out_few, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_few, out_all[:few])
+    packed_np = packed.cpu().numpy()
+    for row in (0, 1, few - 1, rows - 1):
+        n = int(packed_np[row, -1])
+        want = oracle_gqa_row(st.q[row], wl["kv"], st.block_table[int(st.token_to_req[row])],
+                              packed_np[row, :n], spec.page, st.gate[row])
+        ok, err = close_bf16(f64(out_all[row]), want)
+        assert ok, f"row {row}: {err:.3g}"
+
+
 # ----------------------------------------------------------------- full chain
 def _full_chain(spec, wl, st, step, rows=None, packed_ref=None, skip=False):
     """Compare a finished GPU step with the oracle's own chain on `rows`."""
