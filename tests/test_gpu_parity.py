@@ -448,6 +448,53 @@ def test_full_size_sampled_rows(name, nsample):
     print(f"{name}: {n} rows checked, {ties} rows differ only inside the tie window")
 
 
+def test_full_size_decode_batch_fp8_kv_cache():
+    """The decode batch over the FP8-e4m3 main KV cache (static scales) at
+    full size, in the launch configuration the bench times."""
+    spec, step, ties, n = _sampled("decode_batch_fp8kv", 64)
+    assert spec.kv_dtype == W.DTYPE_E4M3
+    assert ties <= max(2, n // 10), f"{ties} tie rows out of {n}"
+
+
+def test_full_size_decode_batch_with_main_prepare():
+    """The decode batch with the main-attention prepare fused into stage 1,
+    at full size: every row's q and gate, its K/V row in the cache, and the
+    whole chain's output against the oracle (stage 4 reads the cache rows
+    this step wrote, which are checked first)."""
+    spec = W.named_spec("decode_batch_prepare")
+    assert spec.main_prep and spec.kv_dtype == W.DTYPE_BF16
+    wl = W.make_workload(spec, device="cuda")
+    st = OracleState(wl, with_kv=False)
+    step = Step(wl, main=True).run()
+    assert Q.check_errors() == 0
+    O.compress_stage(st.cfg, projected_q=None, raw_keys=st.raw_keys, positions=st.positions,
+                     cos_sin=st.cos_sin, q_norm_w=st.q_norm_w, k_norm_w=st.k_norm_w,
+                     ring=st.ring, ring_pos=st.ring_pos, ring_block_table=st.ring_block_table,
+                     token_to_req=st.token_to_req, query_start_loc=st.query_start_loc,
+                     logical_positions=st.logical_positions, ccache=st.ccache,
+                     compressed_slots=st.compressed_slots)
+    m = oracle_main(spec, wl)
+    q = np.zeros((spec.rows, spec.hq, 128))
+    gate = np.zeros_like(q)
+    slots = wl["slot_mapping"].cpu().numpy()
+    blk = torch.as_tensor(slots // spec.page, device="cuda")
+    off = torch.as_tensor(slots % spec.page, device="cuda")
+    got_rows = f64(wl["kv"][blk, :, off, :])  # [rows, Hkv, 2D]
+    for row in range(spec.rows):
+        q[row], gate[row], k, v = O.prepare_main_row(st.cfg, m["qkv"][row], st.positions[row],
+                                                     st.cos_sin, m["q_norm_w"], m["k_norm_w"],
+                                                     m["eps"], spec.hq, spec.hkv)
+        ok, err = close_bf16(got_rows[row, :, :128], k)
+        assert ok, f"K row of row {row}: {err}"
+        np.testing.assert_array_equal(got_rows[row, :, 128:], v)
+    ok, err = close_bf16(f64(wl["main_q_out"]), q)
+    assert ok, f"q: {err}"
+    np.testing.assert_array_equal(f64(wl["main_gate_out"]), gate)
+    st.q, st.gate = q, gate
+    ties = _full_chain(spec, wl, st, step)
+    assert ties <= max(2, spec.rows // 10), f"{ties} tie rows"
+
+
 def test_full_size_invariants_decode_batch():
     """Properties that hold for every row at full size: counts, causality,
     uniqueness, -1 padding."""
