@@ -291,11 +291,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-// Two e4m3 codes (the low and high byte of `v`) -> f16x2, exactly (every
+// The four e4m3 codes of a 32-bit word -> two f16x2 (lo: bytes 0-1, hi:
+// bytes 2-3; the lower byte of a pair in the lower half), exactly (every
 // e4m3 value is an f16 value).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(v));
+}
+// Byte permute of two words (prmt.b32: selector nibbles pick bytes 0-7 of {b, a}).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t out;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(v));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(out) : "r"(a), "r"(b), "r"(sel));
   return out;
 }
 // bf16x2 -> f16x2 (round to nearest; exact for bf16 values inside the f16

@@ -52,19 +52,17 @@ constexpr uint32_t kBadRow = 0xFFFFFFFFu;
 // Shared-memory plan per KV dtype (KVT 0: bf16, 1: e4m3) and ring depth
 // ST.  A warp's stage holds its 16 tokens' K rows, then their V rows, in
 // 16-byte chunks XOR-swizzled by token.  e4m3 rows are half as wide, so the
-// ring is deeper at the same footprint, and each warp has an f16 tile it
-// decodes V into (a 3-stage e4m3 ring at three CTAs per SM measured the
-// same).  bf16 runs 3 stages at two CTAs per SM when the launch is about
-// one wave (HBM latency to hide), 2 stages at three CTAs per SM when it is
-// many waves (prefill: K/V mostly from L2, and more warps to issue).
+// ring is deeper at the same footprint.  bf16 runs 3 stages at two CTAs
+// per SM when the launch is about one wave (HBM latency to hide), 2 stages
+// at three CTAs per SM when it is many waves (prefill: K/V mostly from L2,
+// and more warps to issue).
 template <int KVT, int ST>
 struct KvPlan {
   static constexpr int kRowB = KVT ? 256 : 512;          // K|V bytes of one (token, KV head)
   static constexpr int kStages = ST;
   static constexpr int kSlab = 16 * kRowB;                // bytes per warp stage
   static constexpr int kPipe = kWarps * kStages * kSlab;
-  static constexpr int kVf16 = KVT ? kWarps * 16 * 256 : 0;  // per-warp f16 V tiles
-  static constexpr int kSmem = kPipe + kVf16 + kMaxTok * 4;
+  static constexpr int kSmem = kPipe + kMaxTok * 4;
 };
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -136,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_vmask[kWarps][kStages];
   __shared__ int s_last;
-  uint32_t* s_rowid = reinterpret_cast<uint32_t*>(smem + KP::kPipe + KP::kVf16);
+  uint32_t* s_rowid = reinterpret_cast<uint32_t*>(smem + KP::kPipe);
   const uint8_t* kvb = static_cast<const uint8_t*>(P.kv);
   // KV-head-major CTA order: the CTAs resident at one time mostly share a
   // KV head, so the rows of a request that select the same tokens (prefill
@@ -386,10 +384,11 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
           const int rl = lane & 15;
           const int ch = 2 * k2 + (lane >> 4);
           ldmatrix_x4(a, sK + rl * 128 + ((ch ^ (rl & 7)) << 4));
-          const uint32_t fa[4] = {e4m3x2_to_f16x2(a[0] & 0xFFFFu), e4m3x2_to_f16x2(a[1] & 0xFFFFu),
-                                  e4m3x2_to_f16x2(a[0] >> 16), e4m3x2_to_f16x2(a[1] >> 16)};
-          const uint32_t fb[4] = {e4m3x2_to_f16x2(a[2] & 0xFFFFu), e4m3x2_to_f16x2(a[3] & 0xFFFFu),
-                                  e4m3x2_to_f16x2(a[2] >> 16), e4m3x2_to_f16x2(a[3] >> 16)};
+          uint32_t fa[4], fb[4];
+          e4m3x4_to_f16x2x2(a[0], fa[0], fa[2]);
+          e4m3x4_to_f16x2x2(a[1], fa[1], fa[3]);
+          e4m3x4_to_f16x2x2(a[2], fb[0], fb[2]);
+          e4m3x4_to_f16x2x2(a[3], fb[1], fb[3]);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
             mma_f16_16816(sa[nb][(2 * k2) & 3], fa, qb[nb][2 * k2][0], qb[nb][2 * k2][1]);
@@ -442,41 +441,42 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
         pb[nb][0] = movmatrix_trans(KVT ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
         pb[nb][1] = movmatrix_trans(KVT ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
       }
-      const uint8_t* sVt = sV;  // the V rows the transposed loads read (bf16 or f16)
-      if (KVT == 1) {
-        // decode the warp's 16 e4m3 V rows into its f16 tile (same swizzled
-        // layout as a bf16 V block): lane = row (lane & 15), half (lane >> 4)
-        uint8_t* vf = smem + KP::kPipe + warp * 4096;
-        const int j = lane & 15, hf = lane >> 4;
+      if (KVT == 0) {
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int c = 4 * hf + c4;
-          const uint4 raw = *reinterpret_cast<const uint4*>(sV + j * 128 + ((c ^ (j & 7)) << 4));
-          uint4 f0, f1;
-          f0.x = e4m3x2_to_f16x2(raw.x & 0xFFFFu);
-          f0.y = e4m3x2_to_f16x2(raw.x >> 16);
-          f0.z = e4m3x2_to_f16x2(raw.y & 0xFFFFu);
-          f0.w = e4m3x2_to_f16x2(raw.y >> 16);
-          f1.x = e4m3x2_to_f16x2(raw.z & 0xFFFFu);
-          f1.y = e4m3x2_to_f16x2(raw.z >> 16);
-          f1.z = e4m3x2_to_f16x2(raw.w & 0xFFFFu);
-          f1.w = e4m3x2_to_f16x2(raw.w >> 16);
-          *reinterpret_cast<uint4*>(vf + j * 256 + (((2 * c) ^ (j & 7)) << 4)) = f0;
-          *reinterpret_cast<uint4*>(vf + j * 256 + (((2 * c + 1) ^ (j & 7)) << 4)) = f1;
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t a[4];
+          const int tk = (lane & 7) + ((lane >> 4) << 3);
+          const int ch = 2 * mt + ((lane >> 3) & 1);
+          ldmatrix_x4_trans(a, sV + tk * 256 + ((ch ^ (tk & 7)) << 4));
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[nb][mt], a, pb[nb][0], pb[nb][1]);
         }
-        __syncwarp();
-        sVt = vf;
-      }
+      } else {
+        // V^T fragments straight from the e4m3 rows: m-tiles 2P and 2P + 1
+        // take dims 32P + 4g + {0, 1} and {2, 3} in their rows g and g + 8,
+        // so one 32-bit load per token gives a lane its four dims; byte
+        // permutes pair tokens (2t, 2t+1) and (2t+8, 2t+9) per dim before
+        // the e4m3 -> f16 conversion
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        uint32_t a[4];
-        const int tk = (lane & 7) + ((lane >> 4) << 3);
-        const int ch = 2 * mt + ((lane >> 3) & 1);
-        ldmatrix_x4_trans(a, sVt + tk * 256 + ((ch ^ (tk & 7)) << 4));
+        for (int P2 = 0; P2 < 4; ++P2) {
+          const int c = 2 * P2 + (g >> 2);  // 16-byte chunk of dims 32 P2 + 4 g
+          const int bo = (g & 3) * 4;
+          uint32_t w[4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          if (KVT == 0) mma_bf16_16816(o[nb][mt], a, pb[nb][0], pb[nb][1]);
-          else mma_f16_16816(o[nb][mt], a, pb[nb][0], pb[nb][1]);
+          for (int u = 0; u < 4; ++u) {
+            const int tk = 2 * t + (u & 1) + ((u >> 1) << 3);
+            w[u] = *reinterpret_cast<const uint32_t*>(sV + tk * 128 + ((c ^ (tk & 7)) << 4) + bo);
+          }
+          uint32_t a0[4], a1[4];  // m-tiles 2 P2 and 2 P2 + 1
+          e4m3x4_to_f16x2x2(prmt(w[0], w[1], 0x5140u), a0[0], a0[1]);
+          e4m3x4_to_f16x2x2(prmt(w[0], w[1], 0x7362u), a1[0], a1[1]);
+          e4m3x4_to_f16x2x2(prmt(w[2], w[3], 0x5140u), a0[2], a0[3]);
+          e4m3x4_to_f16x2x2(prmt(w[2], w[3], 0x7362u), a1[2], a1[3]);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            mma_f16_16816(o[nb][2 * P2], a0, pb[nb][0], pb[nb][1]);
+            mma_f16_16816(o[nb][2 * P2 + 1], a1, pb[nb][0], pb[nb][1]);
+          }
         }
       }
       __syncwarp();
@@ -509,11 +509,13 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      const int d = 16 * mt + g;
+      // accumulator rows g and g + 8 of m-tile mt -> dims d and d + dd
+      const int d = KVT ? 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) : 16 * mt + g;
+      const int dd = KVT ? 1 : 8;
       co[(hb + 2 * t) * 128 + d] = o[nb][mt][0];
       co[(hb + 2 * t + 1) * 128 + d] = o[nb][mt][1];
-      co[(hb + 2 * t) * 128 + d + 8] = o[nb][mt][2];
-      co[(hb + 2 * t + 1) * 128 + d + 8] = o[nb][mt][3];
+      co[(hb + 2 * t) * 128 + d + dd] = o[nb][mt][2];
+      co[(hb + 2 * t + 1) * 128 + d + dd] = o[nb][mt][3];
     }
   }
   __syncthreads();
