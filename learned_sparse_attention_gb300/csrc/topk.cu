@@ -295,7 +295,7 @@ __device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
 // KPT: keys per thread the loops are unrolled for (4, 8, 16 or 32), the
 // smallest that covers the launch's max_visible with CL * NT threads.
 // NT: 512, or 1024 when there are fewer rows than half the SMs.
-// CL: CTAs per row, one thread-block cluster (1, 2 or 4).  With CL > 1
+// CL: CTAs per row, one thread-block cluster (1 or 2).  With CL > 1
 // the row's blocks are split in order over the cluster's CTAs; each radix
 // pass sums the CTAs' shared histograms through distributed shared memory,
 // so every CTA reaches the same digit, and one exchange of per-CTA counts
@@ -632,15 +632,15 @@ cudaError_t launch_topk_cluster(const TopkParams& p, cudaStream_t stream, bool p
 
 // CTAs per row for rows of more than 4096 keys: 0 = one 1024-thread CTA,
 // else a cluster of that many 512-thread CTAs.  Measured on GB300: many
-// rows gain from pairs while the pairs fit one wave at two CTAs per SM; a
-// few rows of many keys (long-context decode, 8 rows of 16 384 keys) gain
-// ~1 us from four CTAs per row on four SMs; 2 or 8 CTAs per row, and
-// clusters for a decode batch of 64 rows, were slower than one 1024-thread
-// CTA per row.
+// rows gain from pairs while the pairs fit one wave at two CTAs per SM.
+// Fewer rows run one 1024-thread CTA per row: clusters of 2, 4 or 8 per row
+// were slower for the 64-row decode batch, and for the 8-row long-context
+// decode four CTAs per row made about half of the replayed steps ~12 us
+// slower (a two-valued step time; one CTA per row gives one value).
 int topk_cluster_size(int rows, int max_visible, int sms) {
   const long long s = sms > 0 ? sms : 1;
+  (void)max_visible;
   if (rows >= 76) return 2LL * rows <= 2 * s ? 2 : 1;
-  if (4LL * rows <= s && max_visible > 8 * 1024) return 4;
   return 0;
 }
 
@@ -652,7 +652,6 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl) {
     const dim3 b(kRegThreads);
     if (p.max_visible > 4 * 1024) {
       switch (topk_cluster_size(p.rows, p.max_visible, p.sms)) {
-        case 4: return launch_topk_cluster<4>(p, stream, pdl);
         case 2: return launch_topk_cluster<2>(p, stream, pdl);
         case 0: {
           // one 1024-thread CTA per row, half the keys per thread
