@@ -130,7 +130,10 @@ __device__ __forceinline__ void main_prepare_row(const CompressParams& P, int ro
   }
 }
 
-template <int IDT>
+// IDT: indexer dtype (0 bf16, 1 e4m3); NHH: query heads per half-warp
+// (n_heads / 8), so that the query's registers fit the head count: fewer
+// registers, more CTAs per SM for long prefill chunks.
+template <int IDT, int NHH>
 __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
   griddep_launch_dependents();
   if (blockIdx.x >= 2 * P.rows) {  // reads only caller inputs: no wait
@@ -153,13 +156,11 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
   if (!pool) {
     // ---- indexer query: every head of this row, all loads issued first
     if (P.projected_q == nullptr) return;
-    const int nh = P.n_heads >> 3;  // heads per half-warp: 1, 2, 4 or 8
-    float x[8][8];
+    float x[NHH][8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (k < nh)
-        load8_bf16(P.projected_q + (static_cast<long long>(row) * P.n_heads + hw + 8 * k) * kD +
-                       8 * lane16, x[k]);
+    for (int k = 0; k < NHH; ++k)
+      load8_bf16(P.projected_q + (static_cast<long long>(row) * P.n_heads + hw + 8 * k) * kD +
+                     8 * lane16, x[k]);
     int64_t pos[3];
 #pragma unroll
     for (int k = 0; k < 3; ++k)
@@ -170,12 +171,10 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) w1[e] += 1.0f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k < nh) {
-        norm_rope(x[k], w1, P.eps, lane16, c, s);
-        store8<IDT>(P.q_idx,
-                    (static_cast<long long>(row) * P.n_heads + hw + 8 * k) * kD + 8 * lane16, x[k]);
-      }
+    for (int k = 0; k < NHH; ++k) {
+      norm_rope(x[k], w1, P.eps, lane16, c, s);
+      store8<IDT>(P.q_idx,
+                  (static_cast<long long>(row) * P.n_heads + hw + 8 * k) * kD + 8 * lane16, x[k]);
     }
     return;
   }
@@ -255,12 +254,22 @@ __global__ void __launch_bounds__(128) main_prepare_kernel(const CompressParams 
 
 }  // namespace
 
+template <int IDT>
+cudaError_t launch_compress_dt(const CompressParams& p, dim3 grid, cudaStream_t stream, bool pdl) {
+  switch (p.n_heads >> 3) {
+    case 1: return launch_kernel(compress_kernel<IDT, 1>, grid, dim3(128), 0, stream, pdl, p);
+    case 2: return launch_kernel(compress_kernel<IDT, 2>, grid, dim3(128), 0, stream, pdl, p);
+    case 4: return launch_kernel(compress_kernel<IDT, 4>, grid, dim3(128), 0, stream, pdl, p);
+    case 8: return launch_kernel(compress_kernel<IDT, 8>, grid, dim3(128), 0, stream, pdl, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_compress(const CompressParams& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
-  const int grid = (p.main_qkv != nullptr ? 3 : 2) * p.rows;
-  if (p.index_dtype == 1)
-    return launch_kernel(compress_kernel<1>, dim3(grid), dim3(128), 0, stream, pdl, p);
-  return launch_kernel(compress_kernel<0>, dim3(grid), dim3(128), 0, stream, pdl, p);
+  const dim3 grid((p.main_qkv != nullptr ? 3 : 2) * p.rows);
+  if (p.index_dtype == 1) return launch_compress_dt<1>(p, grid, stream, pdl);
+  return launch_compress_dt<0>(p, grid, stream, pdl);
 }
 
 cudaError_t launch_main_prepare(const CompressParams& p, cudaStream_t stream) {
