@@ -324,6 +324,8 @@ qsa_status logits_params(const qsa_cfg* cfg, const void* q_idx, const void* ccac
   p.tma_a = (cfg->cpage >= 8 && static_cast<long long>(cpages) * cfg->cpage < (1ll << 31)) ? 1 : 0;
   p.err = error_word();
   if (p.err == nullptr) return QSA_ERR_CUDA;
+  p.token_to_req = token_to_req;
+  p.remap = (R == 1 && G == 1 && npad <= 64) ? 1 : 0;
 
   const int max_tiles = (max_visible + 127) / 128;
   // Split each row group's key tiles into chunks so that the CTAs with work

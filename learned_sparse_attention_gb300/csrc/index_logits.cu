@@ -85,7 +85,20 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
   // Everything up to griddep_wait reads only caller inputs (metadata, page
   // tables), so it overlaps the tail of the compress kernel.
   const int R = P.rows_per_group;
-  const int4 grp = find_group(P.qsl, P.reqs, P.rows, R * G, blockIdx.x, P.err);
+  int4 grp;
+  int chunk = blockIdx.y;
+  if (P.remap) {  // one row per group: the L-th item that holds keys
+    const int L = blockIdx.y * gridDim.x + blockIdx.x;
+    const int4 rc = find_row_chunk(P.logical, P.rows, P.ratio, P.tiles_per_cta, L);
+    grp = make_int4(rc.x, 1, rc.x >= 0 ? P.token_to_req[rc.x] : 0, 0);
+    chunk = rc.y;
+    if (rc.x >= 0 && (grp.z < 0 || grp.z >= P.reqs)) {
+      if (threadIdx.x == 0) flag_error(P.err);
+      grp.x = -1;
+    }
+  } else {
+    grp = find_group(P.qsl, P.reqs, P.rows, R * G, blockIdx.x, P.err);
+  }
   // The kernels after this one rely on "logits complete" implying "compress
   // complete", so CTA (0, 0) waits for the compress kernel even when it has
   // no work (the other idle CTAs leave at once and free their slots).
@@ -98,7 +111,7 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
   const int p_last = P.logical[row0 + nrows - 1];
   const int vmax = p_last < 0 ? 0 : (p_last + 1) / P.ratio;
   const int total_tiles = (vmax + 127) / 128;
-  const int t_begin = blockIdx.y * P.tiles_per_cta;
+  const int t_begin = chunk * P.tiles_per_cta;
   const int t_end = min(total_tiles, t_begin + P.tiles_per_cta);
   if (t_begin >= t_end) {
     if (keeps_order) griddep_wait();

@@ -73,6 +73,10 @@ struct LogitsParams {
   int row_bytes;
   int tma_a;  // gather the key tiles with one TMA box per compressed page (cpage >= 8)
   int groups_per_cta;  // 1, or 2 (e4m3, N = 256): two row groups share each key tile
+  // one row per group (decode): the CTAs, in launch order, take the (row, key
+  // chunk) items that hold keys, so CTAs without work come last and leave
+  int remap;
+  const int32_t* token_to_req;  // [rows] request of each row (read when remap)
   unsigned long long* err;
 };
 

@@ -116,4 +116,57 @@ __device__ __forceinline__ int4 find_group(const int32_t* qsl, int reqs, int row
   return found;
 }
 
+// The L-th (row, key chunk) item that holds keys, for one row per group:
+// row r has ceil(ceil(vis(r) / 128) / tpc) chunks (vis(r) = its visible
+// compressed keys), items numbered row-major; found by the whole block.
+// Returns (row, chunk, 0, 0), or row = -1 when L is past the last item.
+__device__ __forceinline__ int4 find_row_chunk(const int32_t* logical, int rows, int ratio,
+                                               int tpc, int L) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  __shared__ int4 found;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  if (tid == 0) {
+    carry = 0;
+    found = make_int4(-1, 0, 0, 0);
+  }
+  __syncthreads();
+  for (int base = 0; base < rows; base += blockDim.x) {
+    const int r = base + tid;
+    int nc = 0;
+    if (r < rows) {
+      const int p = logical[r];
+      const int vis = p < 0 ? 0 : (p + 1) / ratio;
+      nc = ((vis + 127) / 128 + tpc - 1) / tpc;
+    }
+    int incl = nc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int v = lane < nwarps ? warp_tot[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += y;
+      }
+      if (lane < nwarps) warp_tot[lane] = v;
+    }
+    __syncthreads();
+    const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - nc;
+    if (r < rows && L >= excl && L < excl + nc) found = make_int4(r, L - excl, 0, 0);
+    __syncthreads();
+    if (tid == 0) carry += warp_tot[nwarps - 1];
+    const bool done = found.x >= 0;
+    __syncthreads();
+    if (done) break;
+  }
+  return found;
+}
+
 }  // namespace qsa
