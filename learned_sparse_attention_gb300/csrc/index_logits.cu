@@ -87,18 +87,21 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
   const int R = P.rows_per_group;
   int4 grp;
   int chunk = blockIdx.y;
-  if (P.remap) {  // one row per group: the L-th item that holds keys
-    const int L = blockIdx.y * gridDim.x + blockIdx.x;
-    const int4 rc = find_row_chunk(P.logical, P.rows, P.ratio, P.tiles_per_cta, L);
-    grp = make_int4(rc.x, 1, rc.x >= 0 ? P.token_to_req[rc.x] : 0, 0);
-    chunk = rc.y;
-    if (rc.x >= 0 && (grp.z < 0 || grp.z >= P.reqs)) {
-      if (threadIdx.x == 0) flag_error(P.err);
-      grp.x = -1;
+  bool remapped = false;
+  if constexpr (NPAD <= 64) {  // (compiled into the narrow kernels only)
+    if (P.remap) {  // one row per group: the L-th item that holds keys
+      const int L = blockIdx.y * gridDim.x + blockIdx.x;
+      const int4 rc = find_row_chunk(P.logical, P.rows, P.ratio, P.tiles_per_cta, L);
+      grp = make_int4(rc.x, 1, rc.x >= 0 ? P.token_to_req[rc.x] : 0, 0);
+      chunk = rc.y;
+      if (rc.x >= 0 && (grp.z < 0 || grp.z >= P.reqs)) {
+        if (threadIdx.x == 0) flag_error(P.err);
+        grp.x = -1;
+      }
+      remapped = true;
     }
-  } else {
-    grp = find_group(P.qsl, P.reqs, P.rows, R * G, blockIdx.x, P.err);
   }
+  if (!remapped) grp = find_group(P.qsl, P.reqs, P.rows, R * G, blockIdx.x, P.err);
   // The kernels after this one rely on "logits complete" implying "compress
   // complete", so CTA (0, 0) waits for the compress kernel even when it has
   // no work (the other idle CTAs leave at once and free their slots).
