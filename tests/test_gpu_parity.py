@@ -56,6 +56,15 @@ MID = {
                                            contexts=(1500, 2603), rows_per_req=(70, 66),
                                            n_heads=8, index_dtype=E4, compress_ratio=4,
                                            token_topk=256, hq=8, hkv=1, page=32),
+    # a decode batch (one row per request) with ragged contexts, rows that
+    # see no compressed key yet among them: the logits CTAs take only the
+    # (row, key chunk) items that hold keys
+    "mid_decode_ragged_e4m3": W.small_spec("mid_decode_ragged_e4m3", seed=30,
+                                           contexts=(3, 2000, 1, 9000, 130, 2, 4500, 700, 64,
+                                                     12000),
+                                           rows_per_req=(1,) * 10, n_heads=32, index_dtype=E4,
+                                           compress_ratio=4, token_topk=256, hq=32, hkv=4,
+                                           page=64),
     # query-head groups other than 8 (the pages only need Hq % Hkv == 0)
     "mid_group16": W.small_spec("mid_group16", seed=19, contexts=(3000, 900, 4100),
                                 rows_per_req=(2, 1, 3), n_heads=16, index_dtype=E4,
