@@ -12,6 +12,12 @@
  *                   selection buffer;
  *   4. sparse GQA-- paged grouped-query attention over the selected tokens,
  *                   with the sigmoid output gate.
+ * Around them: the main-attention prepare (qsa_main_prepare, or fused into
+ * stage 1 through qsa_step_args.main), the k-step MTP draft whose later
+ * steps reuse step 0's selection (qsa_mtp_steps), the fused qkv + indexer
+ * projection GEMM that produces the step's inputs (qsa_qkv_index_proj), and
+ * stage 4 for callers that cannot give it a workspace
+ * (qsa_sparse_gqa_noalloc).
  *
  * Sources: "vllm.models.qwen4_exp.nvidia.qsa" (QSAIndexer.forward and its
  * unfused reference path, Qwen4ExpQSAImpl.forward), "vllm.models.qwen4_exp.
