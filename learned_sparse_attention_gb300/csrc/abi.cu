@@ -679,7 +679,7 @@ qsa_status qsa_qkv_index_proj(const void* x, const void* w, int32_t rows, int32_
   if (p.err == nullptr) return QSA_ERR_CUDA;
   CUtensorMap tw, tx;
   if (!encode_bf16_2d(&tw, w, hidden, ncols, 128) ||
-      !encode_bf16_2d(&tx, x, hidden, rows, proj_tile_rows(rows)))
+      !encode_bf16_2d(&tx, x, hidden, rows, proj_x_box_rows(rows)))
     return QSA_ERR_CUDA;
   return cuda_status(launch_proj_gemm(p, tw, tx, static_cast<cudaStream_t>(stream)));
 }

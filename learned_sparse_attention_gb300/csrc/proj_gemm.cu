@@ -41,7 +41,12 @@ struct ProjCfg {
   static_assert(STAGES >= 3, "ring depth");
 };
 
-template <int BN>
+// MC: the CTA pair of a 2-CTA cluster (adjacent 128-column tiles, the same
+// BN input rows) shares the input tile: each CTA loads half of its rows and
+// multicasts them to both, so a stage costs the SM's TMA unit A + B/2 bytes;
+// a stage is free again once both CTAs' MMAs have read it (the commits are
+// multicast onto both CTAs' empty barriers, which count two arrivals).
+template <int BN, bool MC>
 __global__ void __launch_bounds__(ProjCfg<BN>::THREADS, 1)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const __grid_constant__ CUtensorMap tmap_x, const ProjParams P) {
@@ -61,10 +66,11 @@ __global__ void __launch_bounds__(ProjCfg<BN>::THREADS, 1)
   const int nk = P.hidden / 64;
   unsigned long long* err = P.err;
 
+  const int crank = MC ? static_cast<int>(blockIdx.x & 1) : 0;  // rank in the CTA pair
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], MC ? 2 : 1);
     }
     mbar_init(acc_full, 1);
     fence_barrier_init();
@@ -76,6 +82,7 @@ __global__ void __launch_bounds__(ProjCfg<BN>::THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  if constexpr (MC) cluster_sync_all();  // the peer's barriers exist before any multicast
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
@@ -88,7 +95,21 @@ __global__ void __launch_bounds__(ProjCfg<BN>::THREADS, 1)
         if (!mbar_wait(&empty[s], ph ^ 1u, err)) break;
         mbar_arrive_expect_tx(&full[s], C::STAGE);
         tma_load_2d(sA + s * C::A_STAGE, &tmap_w, kb * 64, n0, &full[s]);
-        tma_load_2d(sB + s * C::B_STAGE, &tmap_x, kb * 64, r0, &full[s]);
+        if constexpr (MC)  // this CTA's half of the input rows, to both CTAs
+          tma_load_2d_multicast(sB + s * C::B_STAGE + crank * (C::B_STAGE / 2), &tmap_x, kb * 64,
+                                r0 + crank * (BN / 2), &full[s], 0x3);
+        else
+          tma_load_2d(sB + s * C::B_STAGE, &tmap_x, kb * 64, r0, &full[s]);
+      }
+      if constexpr (MC) {
+        // every stage released by both CTAs' MMAs before this CTA leaves: no
+        // arrival from the peer may land on a barrier that no longer exists
+        for (int kb = nk; kb < nk + C::STAGES; ++kb) {
+          if (kb - C::STAGES < 0) continue;
+          const int s = kb % C::STAGES;
+          const uint32_t ph = (kb / C::STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, err)) break;
+        }
       }
     }
     __syncwarp();
@@ -110,7 +131,10 @@ __global__ void __launch_bounds__(ProjCfg<BN>::THREADS, 1)
         for (int kk = 0; kk < 4; ++kk)
           umma_f16(tmem, a0 + ((s * C::A_STAGE + kk * 32) >> 4), b0 + ((s * C::B_STAGE + kk * 32) >> 4),
                    idesc, (kb | kk) != 0 ? 1u : 0u);
-        umma_commit(&empty[s]);
+        if constexpr (MC)
+          umma_commit_multicast(&empty[s], 0x3);
+        else
+          umma_commit(&empty[s]);
       }
       umma_commit(acc_full);
     }
@@ -157,13 +181,14 @@ __global__ void __launch_bounds__(ProjCfg<BN>::THREADS, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (MC) cluster_sync_all();  // the peer is done with this CTA's smem
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, BN);
   }
 }
 
-template <int BN>
+template <int BN, bool MC>
 cudaError_t launch_bn(const ProjParams& p, const CUtensorMap& tw, const CUtensorMap& tx,
                       cudaStream_t stream) {
   using C = ProjCfg<BN>;
@@ -171,27 +196,37 @@ cudaError_t launch_bn(const ProjParams& p, const CUtensorMap& tw, const CUtensor
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel<BN>,
+    const cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel<BN, MC>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  const dim3 grid((p.ncols + 127) / 128, (p.rows + BN - 1) / BN);
-  return launch_kernel(proj_gemm_kernel<BN>, grid, dim3(C::THREADS), C::SMEM, stream, false, tw, tx,
-                       p);
+  const int tiles_n = (p.ncols + 127) / 128;
+  if constexpr (MC) {  // pairs of column tiles (an odd last one pairs with an empty tile)
+    const dim3 grid((tiles_n + 1) / 2 * 2, (p.rows + BN - 1) / BN);
+    return launch_kernel_cluster(proj_gemm_kernel<BN, MC>, grid, dim3(C::THREADS), C::SMEM, stream,
+                                 false, 2, tw, tx, p);
+  }
+  const dim3 grid(tiles_n, (p.rows + BN - 1) / BN);
+  return launch_kernel(proj_gemm_kernel<BN, MC>, grid, dim3(C::THREADS), C::SMEM, stream, false, tw,
+                       tx, p);
 }
 
 }  // namespace
 
 int proj_tile_rows(int rows) { return rows <= 64 ? 64 : rows <= 128 ? 128 : 256; }
+int proj_x_box_rows(int rows) {
+  const int t = proj_tile_rows(rows);
+  return t == 256 ? t / 2 : t;
+}
 
 cudaError_t launch_proj_gemm(const ProjParams& p, const CUtensorMap& tmap_w,
                              const CUtensorMap& tmap_x, cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;
   switch (proj_tile_rows(p.rows)) {
-    case 64: return launch_bn<64>(p, tmap_w, tmap_x, stream);
-    case 128: return launch_bn<128>(p, tmap_w, tmap_x, stream);
-    default: return launch_bn<256>(p, tmap_w, tmap_x, stream);
+    case 64: return launch_bn<64, false>(p, tmap_w, tmap_x, stream);
+    case 128: return launch_bn<128, false>(p, tmap_w, tmap_x, stream);
+    default: return launch_bn<256, true>(p, tmap_w, tmap_x, stream);
   }
 }
 

@@ -142,8 +142,11 @@ struct ProjParams {
   unsigned long long* err;
 };
 int proj_tile_rows(int rows);  // input rows per CTA tile (64, 128 or 256)
+// input rows per TMA box: a tile's rows, or half of them for 256-row tiles
+// (whose CTA pairs each load and multicast half)
+int proj_x_box_rows(int rows);
 // tmap_w: [ncols, hidden] bf16, box 64 x 128 rows; tmap_x: [rows, hidden]
-// bf16, box 64 x proj_tile_rows(rows) rows; both 128-byte swizzled.
+// bf16, box 64 x proj_x_box_rows(rows) rows; both 128-byte swizzled.
 cudaError_t launch_proj_gemm(const ProjParams& p, const CUtensorMap& tmap_w,
                              const CUtensorMap& tmap_x, cudaStream_t stream);
 
