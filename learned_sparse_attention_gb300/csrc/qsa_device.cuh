@@ -235,6 +235,11 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
                "r"(src_bytes)
                : "memory");
 }
+// The same without a source size (all 16 bytes valid).
+__device__ __forceinline__ void cp_async16_full(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

@@ -323,13 +323,22 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
       uint8_t* dst_base = smem + (stage * kWarps + warp) * kSlab;
       if (KVT == 0) {  // one 512-byte row per instruction
         const int chunk = lane & 15, is_v = lane >> 4;
+        const uint8_t* src_lane = kvb + is_v * 256 + chunk * 16;
+        if (vm == 0xFFFFu) {  // a full slab (the common case): no per-row masks
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
-          const bool okj = (vm >> j) & 1u;
-          uint8_t* dst = dst_base + is_v * 4096 + j * 256 + ((chunk ^ (j & 7)) << 4);
-          const uint8_t* src = kvb + static_cast<long long>(okj ? rj : 0u) * 512 + is_v * 256 + chunk * 16;
-          cp_async16(dst, src, okj ? 16u : 0u);
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
+            cp_async16_full(dst_base + is_v * 4096 + j * 256 + ((chunk ^ (j & 7)) << 4),
+                            src_lane + static_cast<long long>(rj) * 512);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
+            const bool okj = (vm >> j) & 1u;
+            uint8_t* dst = dst_base + is_v * 4096 + j * 256 + ((chunk ^ (j & 7)) << 4);
+            cp_async16(dst, src_lane + static_cast<long long>(okj ? rj : 0u) * 512, okj ? 16u : 0u);
+          }
         }
       } else {  // two 256-byte rows per instruction
         const int chunk = lane & 7, is_v = (lane >> 3) & 1, sub = lane >> 4;
