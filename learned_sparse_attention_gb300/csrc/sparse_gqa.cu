@@ -342,14 +342,24 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
         }
       } else {  // two 256-byte rows per instruction
         const int chunk = lane & 7, is_v = (lane >> 3) & 1, sub = lane >> 4;
+        const uint8_t* src_lane = kvb + is_v * 128 + chunk * 16;
+        if (vm == 0xFFFFu) {
 #pragma unroll
-        for (int j2 = 0; j2 < 8; ++j2) {
-          const int j = 2 * j2 + sub;
-          const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
-          const bool okj = (vm >> j) & 1u;
-          uint8_t* dst = dst_base + is_v * 2048 + j * 128 + ((chunk ^ (j & 7)) << 4);
-          const uint8_t* src = kvb + static_cast<long long>(okj ? rj : 0u) * 256 + is_v * 128 + chunk * 16;
-          cp_async16(dst, src, okj ? 16u : 0u);
+          for (int j2 = 0; j2 < 8; ++j2) {
+            const int j = 2 * j2 + sub;
+            const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
+            cp_async16_full(dst_base + is_v * 2048 + j * 128 + ((chunk ^ (j & 7)) << 4),
+                            src_lane + static_cast<long long>(rj) * 256);
+          }
+        } else {
+#pragma unroll
+          for (int j2 = 0; j2 < 8; ++j2) {
+            const int j = 2 * j2 + sub;
+            const uint32_t rj = __shfl_sync(0xffffffffu, rid, j);
+            const bool okj = (vm >> j) & 1u;
+            uint8_t* dst = dst_base + is_v * 2048 + j * 128 + ((chunk ^ (j & 7)) << 4);
+            cp_async16(dst, src_lane + static_cast<long long>(okj ? rj : 0u) * 256, okj ? 16u : 0u);
+          }
         }
       }
     };
