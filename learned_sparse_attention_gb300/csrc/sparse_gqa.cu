@@ -12,8 +12,9 @@
 // GB300 mapping.  Decode is an HBM gather: every selected token costs 512
 // contiguous bytes (K then V of one KV head).  One CTA = (row, KV head,
 // split), 4 warps.  Each warp owns 16 tokens of every 64-token tile and runs
-// its own 3-stage cp.async ring over them (16-byte copies, one token row per
-// warp instruction, XOR-swizzled so ldmatrix is conflict-free).  The GQA
+// its own cp.async ring over them (16-byte copies, one token row per warp
+// instruction, XOR-swizzled so ldmatrix is conflict-free); each tile's
+// copies are issued before the previous tile is computed.  The GQA
 // group of query heads is the N = 8 side of m16n8k16 MMAs with the tokens
 // on M (groups of 1 to 8 heads fill one column block, zero queries in the
 // unused columns; groups of 16 take two blocks that share every K and V
@@ -371,7 +372,15 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
     }
     for (int it = 0; it < nt; ++it) {
       cp_async_wait<kStages - 2>();
+      // tile it has landed for every lane, and every lane is done with tile
+      // it - 1, whose stage takes the next copies now: they overlap this
+      // tile's compute
       __syncwarp();
+      {
+        const int nxt = it + kStages - 1;
+        if (nxt < nt) issue(nxt, nxt % kStages);
+        cp_async_commit();
+      }
       const int stage = it % kStages;
       const uint8_t* sK = smem + (stage * kWarps + warp) * kSlab;
       const uint8_t* sV = sK + 8 * KP::kRowB;
@@ -498,10 +507,6 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
           }
         }
       }
-      __syncwarp();
-      const int nxt = it + kStages - 1;
-      if (nxt < nt) issue(nxt, nxt % kStages);
-      cp_async_commit();
     }
     cp_async_wait<0>();
   }
