@@ -23,7 +23,9 @@
 //   O^T[128 dims x 8 heads] += V^T[128 x 16] . P^T       (8 m-tiles)
 // P^T comes from the S^T accumulator with one movmatrix transpose per 8x8
 // block; each lane keeps the online-softmax state of its two heads, the same
-// heads its O^T fragments hold.  The four warps are merged in shared memory.
+// heads its O^T fragments hold.  The state's reference max moves only when a
+// score passes it by a margin, so most slabs skip the max reduction and the
+// rescale.  The four warps are merged in shared memory.
 // A prologue resolves the CTA's token range (packed index -> block table ->
 // KV row id, in chunks of up to 2560 tokens) into shared memory in parallel,
 // so the copy issue of a slab never waits on a dependent global load; the
@@ -66,6 +68,9 @@ struct KvPlan {
   static constexpr int kSmem = kPipe + kMaxTok * 4;
 };
 constexpr float kLog2e = 1.4426950408889634f;
+// A head's softmax reference moves only when a score passes it by more than
+// this (log2 units): the exponentials stay <= 256, well inside bf16 / f16.
+constexpr float kLazy = 8.0f;
 
 __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
 
@@ -436,22 +441,23 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
         const float x1 = v0 ? sc[1] * sl2 : -INFINITY;  // token g,   head 2t+1
         const float x2 = v1 ? sc[2] * sl2 : -INFINITY;  // token g+8, head 2t
         const float x3 = v1 ? sc[3] * sl2 : -INFINITY;  // token g+8, head 2t+1
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        // m0 / m1 are each head's reference for the exponentials, not its
+        // exact running max: they move (with the max reduction over the
+        // warp and the rescale of the sums and the accumulator) only when
+        // some score exceeds its head's reference by more than kLazy, so
+        // every p stays <= 2^kLazy; m, l and o stay consistent with one
+        // another, which is all the merges and the final division use
+        const bool up = fmaxf(x0, x2) > m0[nb] + kLazy || fmaxf(x1, x3) > m1[nb] + kLazy;
+        if (__any_sync(0xffffffffu, up)) {
+          float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m0[nb], mx0), mn1 = fmaxf(m1[nb], mx1);
-        const float b0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float p0 = exp2f(x0 - b0), p1 = exp2f(x1 - b1);
-        const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
-        // the running sums and the accumulator need rescaling only where a
-        // running max grew (the factor is exactly 1 elsewhere): skipped when
-        // no lane's max moved
-        if (__any_sync(0xffffffffu, mn0 != m0[nb] || mn1 != m1[nb])) {
-          const float al0 = exp2f(m0[nb] - b0), al1 = exp2f(m1[nb] - b1);
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          const float mn0 = fmaxf(m0[nb], mx0), mn1 = fmaxf(m1[nb], mx1);
+          const float al0 = exp2f(m0[nb] - (mn0 == -INFINITY ? 0.f : mn0));
+          const float al1 = exp2f(m1[nb] - (mn1 == -INFINITY ? 0.f : mn1));
           l0[nb] *= al0;
           l1[nb] *= al1;
 #pragma unroll
@@ -461,11 +467,15 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
             o[nb][mt][2] *= al0;
             o[nb][mt][3] *= al1;
           }
+          m0[nb] = mn0;
+          m1[nb] = mn1;
         }
+        const float b0 = m0[nb] == -INFINITY ? 0.f : m0[nb];
+        const float b1 = m1[nb] == -INFINITY ? 0.f : m1[nb];
+        const float p0 = exp2f(x0 - b0), p1 = exp2f(x1 - b1);
+        const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
         l0[nb] += p0 + p2;
         l1[nb] += p1 + p3;
-        m0[nb] = mn0;
-        m1[nb] = mn1;
         pb[nb][0] = movmatrix_trans(KVT ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
         pb[nb][1] = movmatrix_trans(KVT ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
       }
