@@ -68,6 +68,13 @@ struct KvPlan {
   static constexpr int kSmem = kPipe + kMaxTok * 4;
 };
 constexpr float kLog2e = 1.4426950408889634f;
+// 2^x by the PTX approximate base-2 exponential, subnormal results flushed
+// to zero (softmax weights that small do not register next to the others).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 // A head's softmax reference moves only when a score passes it by more than
 // this (log2 units): the exponentials stay <= 256, well inside bf16 / f16.
 constexpr float kLazy = 8.0f;
@@ -389,14 +396,14 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
       const int stage = it % kStages;
       const uint8_t* sK = smem + (stage * kWarps + warp) * kSlab;
       const uint8_t* sV = sK + 8 * KP::kRowB;
-      // S^T = K.Q^T over 8 K-steps, split over four accumulators so that the
-      // MMAs form four dependent chains of two instead of one of eight (each
+      // S^T = K.Q^T over 8 K-steps, split over two accumulators so that the
+      // MMAs form two dependent chains of four instead of one of eight (each
       // K fragment feeds every column block)
-      float sa[NB][4][4];
+      float sa[NB][2][4];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) sa[nb][c][0] = sa[nb][c][1] = sa[nb][c][2] = sa[nb][c][3] = 0.f;
+        for (int c = 0; c < 2; ++c) sa[nb][c][0] = sa[nb][c][1] = sa[nb][c][2] = sa[nb][c][3] = 0.f;
       if (KVT == 0) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -405,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
           const int ch = 2 * kk + (lane >> 4);
           ldmatrix_x4(a, sK + rl * 256 + ((ch ^ (rl & 7)) << 4));
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sa[nb][kk & 3], a, qb[nb][kk][0], qb[nb][kk][1]);
+          for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sa[nb][kk & 1], a, qb[nb][kk][0], qb[nb][kk][1]);
         }
       } else {
         // one ldmatrix.x4 brings 32 e4m3 dims of the warp's 16 rows: per lane
@@ -424,8 +431,8 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
           e4m3x4_to_f16x2x2(a[3], fb[1], fb[3]);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
-            mma_f16_16816(sa[nb][(2 * k2) & 3], fa, qb[nb][2 * k2][0], qb[nb][2 * k2][1]);
-            mma_f16_16816(sa[nb][(2 * k2 + 1) & 3], fb, qb[nb][2 * k2 + 1][0], qb[nb][2 * k2 + 1][1]);
+            mma_f16_16816(sa[nb][0], fa, qb[nb][2 * k2][0], qb[nb][2 * k2][1]);
+            mma_f16_16816(sa[nb][1], fb, qb[nb][2 * k2 + 1][0], qb[nb][2 * k2 + 1][1]);
           }
         }
       }
@@ -436,28 +443,34 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
       for (int nb = 0; nb < NB; ++nb) {
         float sc[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[e] = (sa[nb][0][e] + sa[nb][1][e]) + (sa[nb][2][e] + sa[nb][3][e]);
-        const float x0 = v0 ? sc[0] * sl2 : -INFINITY;  // token g,   head 2t
-        const float x1 = v0 ? sc[1] * sl2 : -INFINITY;  // token g,   head 2t+1
-        const float x2 = v1 ? sc[2] * sl2 : -INFINITY;  // token g+8, head 2t
-        const float x3 = v1 ? sc[3] * sl2 : -INFINITY;  // token g+8, head 2t+1
+        for (int e = 0; e < 4; ++e) sc[e] = sa[nb][0][e] + sa[nb][1][e];
         // m0 / m1 are each head's reference for the exponentials, not its
         // exact running max: they move (with the max reduction over the
         // warp and the rescale of the sums and the accumulator) only when
         // some score exceeds its head's reference by more than kLazy, so
         // every p stays <= 2^kLazy; m, l and o stay consistent with one
-        // another, which is all the merges and the final division use
-        const bool up = fmaxf(x0, x2) > m0[nb] + kLazy || fmaxf(x1, x3) > m1[nb] + kLazy;
+        // another, which is all the merges and the final division use.
+        // y: the exponent of each entry (token g / g+8, head 2t / 2t+1)
+        // against its head's reference, +inf while a head has none yet,
+        // -inf for the tokens of a partial slab that are not selected.
+        float y[4] = {fmaf(sc[0], sl2, -m0[nb]), fmaf(sc[1], sl2, -m1[nb]), fmaf(sc[2], sl2, -m0[nb]),
+                      fmaf(sc[3], sl2, -m1[nb])};
+        if (vm != 0xFFFFu) {
+          if (!v0) y[0] = y[1] = -INFINITY;
+          if (!v1) y[2] = y[3] = -INFINITY;
+        }
+        const bool up = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3])) > kLazy;
         if (__any_sync(0xffffffffu, up)) {
-          float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+          float mx0 = fmaxf(v0 ? sc[0] : -INFINITY, v1 ? sc[2] : -INFINITY) * sl2;
+          float mx1 = fmaxf(v0 ? sc[1] : -INFINITY, v1 ? sc[3] : -INFINITY) * sl2;
 #pragma unroll
           for (int off = 4; off < 32; off <<= 1) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
           }
           const float mn0 = fmaxf(m0[nb], mx0), mn1 = fmaxf(m1[nb], mx1);
-          const float al0 = exp2f(m0[nb] - (mn0 == -INFINITY ? 0.f : mn0));
-          const float al1 = exp2f(m1[nb] - (mn1 == -INFINITY ? 0.f : mn1));
+          const float al0 = ex2_ftz(m0[nb] - (mn0 == -INFINITY ? 0.f : mn0));
+          const float al1 = ex2_ftz(m1[nb] - (mn1 == -INFINITY ? 0.f : mn1));
           l0[nb] *= al0;
           l1[nb] *= al1;
 #pragma unroll
@@ -469,11 +482,13 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
           }
           m0[nb] = mn0;
           m1[nb] = mn1;
+          y[0] = v0 ? fmaf(sc[0], sl2, -mn0) : -INFINITY;
+          y[1] = v0 ? fmaf(sc[1], sl2, -mn1) : -INFINITY;
+          y[2] = v1 ? fmaf(sc[2], sl2, -mn0) : -INFINITY;
+          y[3] = v1 ? fmaf(sc[3], sl2, -mn1) : -INFINITY;
         }
-        const float b0 = m0[nb] == -INFINITY ? 0.f : m0[nb];
-        const float b1 = m1[nb] == -INFINITY ? 0.f : m1[nb];
-        const float p0 = exp2f(x0 - b0), p1 = exp2f(x1 - b1);
-        const float p2 = exp2f(x2 - b0), p3 = exp2f(x3 - b1);
+        const float p0 = ex2_ftz(y[0]), p1 = ex2_ftz(y[1]);
+        const float p2 = ex2_ftz(y[2]), p3 = ex2_ftz(y[3]);
         l0[nb] += p0 + p2;
         l1[nb] += p1 + p3;
         pb[nb][0] = movmatrix_trans(KVT ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
