@@ -292,7 +292,7 @@ __device__ __forceinline__ int block_sum_excl(int v, int* scratch, int* total) {
   return ex;
 }
 
-// KPT: keys per thread the loops are unrolled for (4, 8, 16 or 32), the
+// KPT: keys per thread the loops are unrolled for (4, 8, 16, 24 or 32), the
 // smallest that covers the launch's max_visible with CL * NT threads.
 // NT: 512, or 1024 when there are fewer rows than half the SMs.
 // CL: CTAs per row, one thread-block cluster (1 or 2).  With CL > 1
@@ -667,6 +667,7 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream, bool pdl) {
     if (kpt <= 4) return launch_kernel(topk_reg_kernel<4, kRegThreads, 1>, g, b, 0, stream, pdl, p);
     if (kpt <= 8) return launch_kernel(topk_reg_kernel<8, kRegThreads, 1>, g, b, 0, stream, pdl, p);
     if (kpt <= 16) return launch_kernel(topk_reg_kernel<16, kRegThreads, 1>, g, b, 0, stream, pdl, p);
+    if (kpt <= 24) return launch_kernel(topk_reg_kernel<24, kRegThreads, 1>, g, b, 0, stream, pdl, p);
     return launch_kernel(topk_reg_kernel<32, kRegThreads, 1>, g, b, 0, stream, pdl, p);
   }
   const size_t smem = topk_smem_bytes(p.max_visible, p.token_topk / p.ratio);
