@@ -139,8 +139,14 @@ __device__ __forceinline__ uint32_t kv_row_id(const GqaParams& P, int off, int p
 // NB: column blocks of 8 query heads (1 for groups of 1-8, 2 for 16).
 // KVT: KV cache dtype, 0 bf16, 1 e4m3 with static scales (f16 MMAs: every
 // e4m3 value and every bf16 query of normal range is exact in f16).
-template <int NB, int KVT, int ST>
+// ROW: one CTA per row, warp w taking KV head w over all the row's tokens
+// (four KV heads, no split): the row's selection is resolved once for its
+// four KV heads and each warp finishes its own heads, with no merge across
+// warps.  Used for launches of many waves, where a CTA's fixed costs
+// (resolving the selection, the ring's fill and drain, the merge) weigh.
+template <int NB, int KVT, int ST, bool ROW>
 __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
+  static_assert(!ROW || (NB == 1 && KVT == 0), "row CTAs: bf16 KV, groups of up to 8 heads");
   using KP = KvPlan<KVT, ST>;
   constexpr int kStages = KP::kStages;
   constexpr int kSlab = KP::kSlab;
@@ -149,14 +155,16 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   __shared__ int s_last;
   uint32_t* s_rowid = reinterpret_cast<uint32_t*>(smem + KP::kPipe);
   const uint8_t* kvb = static_cast<const uint8_t*>(P.kv);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // KV-head-major CTA order: the CTAs resident at one time mostly share a
   // KV head, so the rows of a request that select the same tokens (prefill
   // chunks, speculative rows) find them in L2
-  const int kvh = blockIdx.x / P.rows;
-  const int row = blockIdx.x - kvh * P.rows;
+  const int kvh = ROW ? warp : static_cast<int>(blockIdx.x) / P.rows;
+  const int row = ROW ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) - kvh * P.rows;
   const int pair = row * P.hkv + kvh;  // merge ticket of this (row, KV head)
   const int split = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // row CTAs resolve KV head 0's row ids; warp w's rows are page * w further
+  const uint8_t* kvw = kvb + (ROW ? static_cast<long long>(warp) * P.page * KP::kRowB : 0ll);
   const int g = lane >> 2, t = lane & 3;
   const int Wcols = P.packed_width - 1;
 
@@ -209,16 +217,18 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
         if (i0 + u * kThreads < P.bt_stride) s_bt[i0 + u * kThreads] = v[u];
     }
   }
-  // the epilogue's items of this thread (item tid + 128 nb: head item / 16 of
-  // the group, 8 dims) and their gate (a caller input)
-  const int d0 = (threadIdx.x & 15) * 8;   // 8 dims per item
-  uint4 gate8[NB];
+  // the epilogue's items of this thread, 8 dims each, and their gate (a
+  // caller input): item tid + 128 i is head item / 16 of the group; with row
+  // CTAs a warp finishes its own 8 heads, lane + 32 i being head item / 16
+  constexpr int NI = ROW ? 4 : NB;
+  const int d0 = (threadIdx.x & 15) * 8;
+  uint4 gate8[NI];
   auto load_gates = [&]() {
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const int hh = (threadIdx.x + kThreads * nb) >> 4;
-      gate8[nb] = hh < G ? load_gate8(P, (static_cast<long long>(row) * P.hq + kvh * G + hh) * 128 + d0)
-                         : make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < NI; ++i) {
+      const int hh = ROW ? (lane + 32 * i) >> 4 : (threadIdx.x + kThreads * i) >> 4;
+      gate8[i] = hh < G ? load_gate8(P, (static_cast<long long>(row) * P.hq + kvh * G + hh) * 128 + d0)
+                        : make_uint4(0u, 0u, 0u, 0u);
     }
   };
   if (!P.q_after_wait) {
@@ -292,7 +302,7 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
     for (int u = 0; u < NT; ++u) {
       const int i = i0 + u * kThreads;
       if (i >= cn) continue;
-      const uint32_t rid = kv_row_id(P, off[u], pid[u], kvh);
+      const uint32_t rid = kv_row_id(P, off[u], pid[u], ROW ? 0 : kvh);
       bad |= rid == kBadRow;
       s_rowid[i] = rid;
     }
@@ -314,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   // before the chunk's copies start.
   for (int c0 = 0; c0 < ntok; c0 += kMaxTok) {
     const int cn = min(kMaxTok, ntok - c0);
-    const int nt = (cn + kTile - 1) / kTile;
+    const int nt = ROW ? (cn + 15) / 16 : (cn + kTile - 1) / kTile;  // slabs of this warp
     if (c0 > 0) __syncthreads();  // every warp has issued the previous chunk's copies
     const int i_begin = c0 == 0 ? kFirst * kThreads : 0;
     for (int i0 = i_begin + threadIdx.x; i0 < cn; i0 += kRidBatch * kThreads) {
@@ -329,14 +339,14 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
     __syncthreads();  // all row ids of the chunk are resolved
 
     auto issue = [&](int tile, int stage) {
-      const int li = tile * kTile + warp * 16 + (lane & 15);
+      const int li = (ROW ? tile * 16 : tile * kTile + warp * 16) + (lane & 15);
       const uint32_t rid = (lane < 16 && li < cn) ? s_rowid[li] : kBadRow;
       const uint32_t vm = __ballot_sync(0xffffffffu, rid != kBadRow) & 0xffffu;
       if (lane == 0) s_vmask[warp][stage] = vm;
       uint8_t* dst_base = smem + (stage * kWarps + warp) * kSlab;
       if (KVT == 0) {  // one 512-byte row per instruction
         const int chunk = lane & 15, is_v = lane >> 4;
-        const uint8_t* src_lane = kvb + is_v * 256 + chunk * 16;
+        const uint8_t* src_lane = kvw + is_v * 256 + chunk * 16;
         if (vm == 0xFFFFu) {  // a full slab (the common case): no per-row masks
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -355,7 +365,7 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
         }
       } else {  // two 256-byte rows per instruction
         const int chunk = lane & 7, is_v = (lane >> 3) & 1, sub = lane >> 4;
-        const uint8_t* src_lane = kvb + is_v * 128 + chunk * 16;
+        const uint8_t* src_lane = kvw + is_v * 128 + chunk * 16;
         if (vm == 0xFFFFu) {
 #pragma unroll
           for (int j2 = 0; j2 < 8; ++j2) {
@@ -537,6 +547,39 @@ __global__ void __launch_bounds__(kThreads) gqa_kernel(const GqaParams P) {
   }
   if (bad) flag_error(P.err);
 
+  if constexpr (ROW) {
+    // the warp's 8 heads, normalised, through its own first ring stage (its
+    // copies have all landed) to 16-byte stores with the gate
+    __syncwarp();
+    float* co = reinterpret_cast<float*>(smem + warp * kSlab);  // [8 heads][128 dims]
+    float la = l0[0], lb = l1[0];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      la += __shfl_xor_sync(0xffffffffu, la, off);
+      lb += __shfl_xor_sync(0xffffffffu, lb, off);
+    }
+    const float ia = la > 0.f ? 1.0f / la : 0.f, ib = lb > 0.f ? 1.0f / lb : 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d = 16 * mt + g;  // accumulator rows g and g + 8 of m-tile mt
+      co[(2 * t) * 128 + d] = o[0][mt][0] * ia;
+      co[(2 * t + 1) * 128 + d] = o[0][mt][1] * ib;
+      co[(2 * t) * 128 + d + 8] = o[0][mt][2] * ia;
+      co[(2 * t + 1) * 128 + d + 8] = o[0][mt][3] * ib;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int hh = (lane + 32 * i) >> 4;
+      if (hh >= G) continue;
+      const float4 a = *reinterpret_cast<const float4*>(co + hh * 128 + d0);
+      const float4 b = *reinterpret_cast<const float4*>(co + hh * 128 + d0 + 4);
+      const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      store_out8(P, (static_cast<long long>(row) * P.hq + kvh * G + hh) * 128 + d0, x, gate8[i]);
+    }
+    return;
+  }
+
   __syncthreads();  // pipeline buffers are free from here on
   float* cm = reinterpret_cast<float*>(smem);   // [warps][8 NB] max
   float* cl = cm + kWarps * 8 * NB;             // [warps][8 NB] sum
@@ -660,17 +703,23 @@ cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
     return cudaErrorInvalidValue;
   if (p.group < 1 || (p.group > 8 && p.group != 16)) return cudaErrorInvalidValue;
   if (p.kv_dtype != 0 && p.kv_dtype != 1) return cudaErrorInvalidValue;
-  // kernels by [column blocks][ring plan: bf16 3 stages, bf16 2 stages, e4m3 5 stages]
-  void (*kerns[2][3])(const GqaParams) = {
-      {gqa_kernel<1, 0, 3>, gqa_kernel<1, 0, 2>, gqa_kernel<1, 1, 5>},
-      {gqa_kernel<2, 0, 3>, gqa_kernel<2, 0, 2>, gqa_kernel<2, 1, 5>}};
-  const int smems[3] = {KvPlan<0, 3>::kSmem, KvPlan<0, 2>::kSmem, KvPlan<1, 5>::kSmem};
+  // kernels by [column blocks][ring plan: bf16 3 stages, bf16 2 stages,
+  // e4m3 5 stages, bf16 2 stages with row CTAs]
+  void (*kerns[2][4])(const GqaParams) = {
+      {gqa_kernel<1, 0, 3, false>, gqa_kernel<1, 0, 2, false>, gqa_kernel<1, 1, 5, false>,
+       gqa_kernel<1, 0, 2, true>},
+      {gqa_kernel<2, 0, 3, false>, gqa_kernel<2, 0, 2, false>, gqa_kernel<2, 1, 5, false>,
+       gqa_kernel<2, 0, 2, false>}};
+  const int smems[4] = {KvPlan<0, 3>::kSmem, KvPlan<0, 2>::kSmem, KvPlan<1, 5>::kSmem,
+                        KvPlan<0, 2>::kSmem};
   const int ki = p.group <= 8 ? 0 : 1;
   const long long ctas = static_cast<long long>(p.rows) * p.hkv * p.splits;
-  const int plan = p.kv_dtype == 1 ? 2 : (ctas > 4ll * (p.sms > 0 ? p.sms : 1) ? 1 : 0);
+  const bool many = ctas > 4ll * (p.sms > 0 ? p.sms : 1);
+  int plan = p.kv_dtype == 1 ? 2 : many ? 1 : 0;
+  if (plan == 1 && ki == 0 && p.hkv == kWarps && p.splits == 1) plan = 3;
   auto kern = kerns[ki][plan];
   const int kSmem = smems[plan];
-  static bool attr_set[2][3][64] = {};
+  static bool attr_set[2][4][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[ki][plan][dev]) {
@@ -685,8 +734,8 @@ cudaError_t launch_sparse_gqa(const GqaParams& p, cudaStream_t stream, bool pdl,
     if (e != cudaSuccess) return e;
     pdl = false;  // a memset node sits between this kernel and its predecessor
   }
-  cudaError_t e = launch_kernel(kern, dim3(p.rows * p.hkv, p.splits), dim3(kThreads), kSmem,
-                                stream, pdl, p);
+  const dim3 grid = plan == 3 ? dim3(p.rows, 1) : dim3(p.rows * p.hkv, p.splits);
+  cudaError_t e = launch_kernel(kern, grid, dim3(kThreads), kSmem, stream, pdl, p);
   if (e != cudaSuccess || p.splits == 1 || p.counters != nullptr) return e;
   return launch_kernel(gqa_merge_kernel, dim3(p.rows), dim3(256), 0, stream, true, p);
 }

@@ -299,15 +299,21 @@ def test_split_kv_invariance():
         assert ok, err
 
 
-def test_ring_plans_agree():
+@pytest.mark.parametrize("hq,hkv", [(32, 4), (64, 8)])
+def test_ring_plans_agree(hq, hkv):
     """Stage 4 runs a 3-stage ring at two CTAs per SM for launches of about
-    one wave and a 2-stage ring at three CTAs per SM for many waves; the
-    arithmetic is the same, so rows computed in a many-wave launch equal the
-    same rows computed in a small launch bit for bit."""
+    one wave and a 2-stage ring at three CTAs per SM for many waves; with
+    four KV heads the many-wave launch takes one CTA per row (a warp per KV
+    head over all the row's tokens) instead of one per (row, KV head) (four
+    warps over a quarter of the tokens each, merged).  Rows computed in a
+    many-wave launch equal the same rows computed in a small launch: bit for
+    bit where the arithmetic is the same (eight KV heads), within the bf16
+    tolerance where the order of the sums differs (four), and every plan
+    matches the oracle."""
     rows = 720
     spec = W.small_spec("plans", seed=31, contexts=[2500] * rows, rows_per_req=[1] * rows,
                         n_heads=8, index_dtype=BF, compress_ratio=4, token_topk=256,
-                        hq=32, hkv=4, page=64)
+                        hq=hq, hkv=hkv, page=64)
     wl = W.make_workload(spec, device="cuda")
     _, gcfg = cfgs(spec, wl)
     assert Q.gqa_splits(gcfg, rows, spec.packed_width) == 1
@@ -319,21 +325,26 @@ def test_ring_plans_agree():
     out_all = torch.empty_like(wl["q"])
     Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], packed, wl["token_to_req"],
                  wl["gate"], out_all, ws)
-    few = 60  # 240 CTAs: the one-wave plan
+    few = 60  # at most 480 CTAs: the one-wave plan
     assert Q.gqa_splits(gcfg, few, spec.packed_width) == 1
     out_few = torch.empty_like(wl["q"][:few])
     Q.sparse_gqa(gcfg, wl["q"][:few].contiguous(), wl["kv"], wl["block_table"],
                  packed[:few].contiguous(), wl["token_to_req"][:few].contiguous(),
                  wl["gate"][:few].contiguous(), out_few, ws)
     torch.cuda.synchronize()
-    assert torch.equal(out_few, out_all[:few])
+    if hkv == 4:
+        ok, err = close_bf16(f64(out_all[:few]), f64(out_few))
+        assert ok, err
+    else:
+        assert torch.equal(out_few, out_all[:few])
     packed_np = packed.cpu().numpy()
-    for row in (0, 1, few - 1, rows - 1):
+    for row in (0, 1, 2, few - 1, rows // 2, rows - 1):
         n = int(packed_np[row, -1])
         want = oracle_gqa_row(st.q[row], wl["kv"], st.block_table[int(st.token_to_req[row])],
                               packed_np[row, :n], spec.page, st.gate[row])
-        ok, err = close_bf16(f64(out_all[row]), want)
-        assert ok, f"row {row}: {err:.3g}"
+        for got in (out_all[row],) + ((out_few[row],) if row < few else ()):
+            ok, err = close_bf16(f64(got), want)
+            assert ok, f"row {row}: {err:.3g}"
 
 
 # ----------------------------------------------------------------- full chain
