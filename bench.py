@@ -57,7 +57,7 @@ def flush_l2(flush, drain, i):
 # DRAM bytes per launch of the sparse GQA kernel on the decode batch, from one
 # ncu capture (the decode-batch kernel-sections summary), keyed by a hash of
 # the kernel sources it was taken on; any other source reports null.
-GQA_TRAFFIC = {"edf7e2bfa9db410d": 270435072 + 3398912}
+GQA_TRAFFIC = {"3d78878b20f11825": 270419968 + 3646464}
 GQA_SOURCES = ("learned_sparse_attention_gb300/csrc/sparse_gqa.cu",
                "learned_sparse_attention_gb300/csrc/qsa_device.cuh")
 
