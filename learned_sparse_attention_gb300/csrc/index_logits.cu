@@ -101,7 +101,11 @@ __global__ void __launch_bounds__(LogitsCfg<IDT, NPAD, G, TMA>::THREADS, 1)
       remapped = true;
     }
   }
-  if (!remapped) grp = find_group(P.qsl, P.reqs, P.rows, R * G, blockIdx.x, P.err);
+  // Wide kernels (prefill-sized row groups) take the groups last-first: the
+  // later groups of a causal chunk see more keys, so the longest CTAs start
+  // in the first wave and the last wave holds the shortest ones.
+  const int gidx = NPAD >= 128 ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  if (!remapped) grp = find_group(P.qsl, P.reqs, P.rows, R * G, gidx, P.err);
   // The kernels after this one rely on "logits complete" implying "compress
   // complete", so CTA (0, 0) waits for the compress kernel even when it has
   // no work (the other idle CTAs leave at once and free their slots).
