@@ -239,11 +239,13 @@ def test_sparse_gqa_matches_oracle(name, gate):
     assert (got[-1] == 0).all()
 
 
-@pytest.mark.parametrize("hq,hkv", [(32, 4), (32, 2)])
+@pytest.mark.parametrize("hq,hkv", [(32, 4), (32, 2), (8, 4), (16, 4)])
 def test_sparse_gqa_many_rows_ragged(hq, hkv):
     """Many (row, KV head) pairs (the prefill shape: several waves of CTAs,
     no split-KV), with ragged selections: counts from 0 to the full width,
-    and rows whose selection is the whole prefix."""
+    and rows whose selection is the whole prefix.  Four KV heads take one
+    CTA per row (a warp per KV head), also with groups of 2 and 4 query
+    heads; two KV heads (groups of 16) one CTA per (row, KV head)."""
     rows = 1400
     rng = np.random.default_rng(hq + hkv)
     contexts = [int(x) for x in rng.integers(5, 400, size=rows)]
