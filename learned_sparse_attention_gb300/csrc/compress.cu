@@ -146,15 +146,15 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
   const int row = pool ? b - P.rows : b;
   const int hw = threadIdx.x >> 4;       // half-warp 0..7
   const int lane16 = threadIdx.x & 15;   // dims 8*lane16 .. +7
+  // the row's metadata in one round trip (the pooling CTAs' slot with it)
   const int req = P.token_to_req[row];
   const int p = P.logical[row];
-  if (req < 0 || req >= P.reqs) {
-    if (pool && threadIdx.x == 0) flag_error(P.err);
-    return;
-  }
+  const long long slot = pool ? P.slots[row] : -1;
 
   if (!pool) {
     // ---- indexer query: every head of this row, all loads issued first
+    // (they read only this row's caller inputs, so they go out before the
+    // request id is checked)
     if (P.projected_q == nullptr) return;
     float x[NHH][8];
 #pragma unroll
@@ -166,8 +166,9 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
     for (int k = 0; k < 3; ++k)
       pos[k] = P.positions[static_cast<long long>(row) * 3 + (P.mrope ? k : 0)];
     float c[8], s[8], w1[8];
-    rope_coeffs(rope_params(P), lane16, pos, c, s);
     load8_bf16(P.q_norm_w + 8 * lane16, w1);
+    if (req < 0 || req >= P.reqs) return;
+    rope_coeffs(rope_params(P), lane16, pos, c, s);
 #pragma unroll
     for (int e = 0; e < 8; ++e) w1[e] += 1.0f;
 #pragma unroll
@@ -182,16 +183,19 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
   // ---- group completed by this row: pool, norm, rotate, cast, store.
   // Warp 0 runs it; both of its half-warps compute the same key (the
   // shuffles stay inside a half-warp) and half-warp 0 stores it.
-  const long long slot = P.slots[row];
+  if (req < 0 || req >= P.reqs) {
+    if (threadIdx.x == 0) flag_error(P.err);
+    return;
+  }
   if (slot < 0 || (threadIdx.x >> 5) != 0) return;
   const int r = P.ratio;
   const int first_row = P.qsl[req];
+  const int ring_block = P.ring_bt[static_cast<long long>(req) * P.ring_bt_stride];
   if (first_row < 0 || first_row > row) {  // inconsistent query_start_loc
     if (threadIdx.x == 0) flag_error(P.err);
     return;
   }
   const int step_start = P.logical[first_row];
-  const int ring_block = P.ring_bt[static_cast<long long>(req) * P.ring_bt_stride];
   const long long nslots = static_cast<long long>(P.cpages) * P.cpage;
   const int t0 = p - r + 1;
   const bool ring_needed = t0 < step_start;
@@ -202,19 +206,32 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
     if (threadIdx.x == 0) flag_error(P.err);
     return;
   }
+  // The group's keys go out 8 at a time (one round trip for r <= 8) and
+  // are summed in position order, together with the RoPE position's loads.
+  uint4 kr[8];
+  auto load_keys = [&](int tb) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = tb + u;
+      if (t > p) continue;
+      const uint16_t* src =
+          t >= step_start ? P.raw_keys + static_cast<long long>(first_row + (t - step_start)) * kD
+                          : P.ring + (static_cast<long long>(ring_block) * P.S + (t % P.S)) * kD;
+      kr[u] = *reinterpret_cast<const uint4*>(src + 8 * lane16);
+    }
+  };
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int t = t0; t <= p; ++t) {
-    const uint16_t* src =
-        t >= step_start ? P.raw_keys + static_cast<long long>(first_row + (t - step_start)) * kD
-                        : P.ring + (static_cast<long long>(ring_block) * P.S + (t % P.S)) * kD;
-    float x[8];
-    load8_bf16(src + 8 * lane16, x);
+  auto sum_keys = [&](int tb) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += x[e];
-  }
-  const float inv_r = 1.0f / static_cast<float>(r);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] *= inv_r;
+    for (int u = 0; u < 8; ++u) {
+      if (tb + u > p) continue;
+      acc[0] += bf16_lo(kr[u].x); acc[1] += bf16_hi(kr[u].x);
+      acc[2] += bf16_lo(kr[u].y); acc[3] += bf16_hi(kr[u].y);
+      acc[4] += bf16_lo(kr[u].z); acc[5] += bf16_hi(kr[u].z);
+      acc[6] += bf16_lo(kr[u].w); acc[7] += bf16_hi(kr[u].w);
+    }
+  };
+  load_keys(t0);
 
   int64_t pos[3];
   if (!P.mrope) {
@@ -229,8 +246,16 @@ __global__ void __launch_bounds__(128) compress_kernel(const CompressParams P) {
     for (int k = 0; k < 3; ++k) pos[k] = P.ring_pos[ring_slot * 3 + k];
   }
   float c[8], s[8], w1[8];
-  rope_coeffs(rope_params(P), lane16, pos, c, s);
   load8_bf16(P.k_norm_w + 8 * lane16, w1);
+  rope_coeffs(rope_params(P), lane16, pos, c, s);
+  sum_keys(t0);
+  for (int tb = t0 + 8; tb <= p; tb += 8) {
+    load_keys(tb);
+    sum_keys(tb);
+  }
+  const float inv_r = 1.0f / static_cast<float>(r);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] *= inv_r;
 #pragma unroll
   for (int e = 0; e < 8; ++e) w1[e] += 1.0f;
   norm_rope(acc, w1, P.eps, lane16, c, s);

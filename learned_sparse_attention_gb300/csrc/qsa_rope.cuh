@@ -61,7 +61,9 @@ __device__ __forceinline__ void rope_coeffs(const RopeParams& P, int lane16,
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int i = fbase + e;
-    int64_t pp = pos[mrope_component(i, P.mrope, P.sec_h, P.sec_w)];
+    // (a select, not an index: pos stays in registers)
+    const int comp = mrope_component(i, P.mrope, P.sec_h, P.sec_w);
+    int64_t pp = comp == 0 ? pos[0] : comp == 1 ? pos[1] : pos[2];
     if (pp < 0 || pp >= P.max_pos) {
       if (lane16 == 0 && e == 0) flag_error(P.err);
       pp = pp < 0 ? 0 : P.max_pos - 1;
