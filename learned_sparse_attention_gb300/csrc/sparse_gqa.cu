@@ -25,7 +25,10 @@
 // block; each lane keeps the online-softmax state of its two heads, the same
 // heads its O^T fragments hold.  The state's reference max moves only when a
 // score passes it by a margin, so most slabs skip the max reduction and the
-// rescale.  The four warps are merged in shared memory.
+// rescale.  The four warps are merged in shared memory.  Launches of many
+// waves with four KV heads (a prefill chunk) take one CTA per row instead:
+// warp w runs KV head w over all the row's tokens in the same way and
+// finishes its own heads, with no merge.
 // A prologue resolves the CTA's token range (packed index -> block table ->
 // KV row id, in chunks of up to 2560 tokens) into shared memory in parallel,
 // so the copy issue of a slab never waits on a dependent global load; the
