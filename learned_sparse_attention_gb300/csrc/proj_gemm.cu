@@ -3,8 +3,8 @@
 // fp32 accumulator rounded once to bf16 and written to three outputs.
 //
 // Follows "vllm.models.qwen4_exp.nvidia.qsa": Qwen4ExpQSAQKVIndexerLinear
-// (the indexer's index_qk_proj packed as shard 3 of the qkv GEMM: "Pack
-// sharded Q/gate, K, V and replicated indexer Q/K in one GEMM"),
+// (the indexer's index_qk_proj packed as shard 3 of the qkv GEMM, so one
+// GEMM yields the sharded Q/gate, K and V and the replicated indexer Q/K),
 // Qwen4ExpQSAAttention.forward (qkv, projected_qk = qkv.split([2 q_size +
 // 2 kv_size, index_qk_size])) and QSAIndexer.forward (projected_q,
 // raw_keys = projected_qk.split((index_n_heads D, index_kv_heads D))).

@@ -299,7 +299,7 @@ def compress_key(cfg: QsaConfig, member_keys, first_pos3, cos_sin, k_norm_w) -> 
     one rounding (R2).
 
     Follows "vllm.models.qwen4_exp.nvidia.ops.qsa",
-    qsa_compress_groups_with_ratio ("Pool completed groups ..."), then the
+    qsa_compress_groups_with_ratio (completed groups are pooled), then the
     unfused path's gemma_rmsnorm / apply_qsa_rope(first_positions) /
     qsa_store_cache_rows.  member_keys: [r, D].
     """
@@ -421,8 +421,8 @@ def qkv_index_projection(x, w, qkv_cols: int, index_q_cols: int):
     projected_q, its raw keys).
 
     Follows "vllm.models.qwen4_exp.nvidia.qsa": Qwen4ExpQSAQKVIndexerLinear
-    ("Pack sharded Q/gate, K, V and replicated indexer Q/K in one GEMM",
-    the indexer's weights as shard 3), Qwen4ExpQSAAttention.forward (qkv,
+    (sharded Q/gate, K and V and the replicated indexer Q/K computed by one
+    GEMM, the indexer's weights as shard 3), Qwen4ExpQSAAttention.forward (qkv,
     projected_qk = qkv.split([2 * q_size + 2 * kv_size, index_qk_size])) and
     QSAIndexer.forward (projected_q, raw_keys = projected_qk.split(
     (index_n_heads * D, index_kv_heads * D))).  x: [rows, hidden]; w:
