@@ -349,6 +349,39 @@ def test_ring_plans_agree(hq, hkv):
             assert ok, f"row {row}: {err:.3g}"
 
 
+def test_many_wave_long_selections_split_and_merged():
+    """A prefill-shaped launch (many rows, four KV heads) whose selections
+    are longer than one chunk of staged row ids (4099 > 2560 entries): the
+    split count keeps every CTA within one chunk, so it takes two splits per
+    (row, KV head), merged by the last CTA, instead of one CTA per row."""
+    rows_per, reqs = 60, 12
+    spec = W.small_spec("row_chunks", seed=41, contexts=[6000] * reqs, rows_per_req=[rows_per] * reqs,
+                        n_heads=8, index_dtype=BF, compress_ratio=4, token_topk=4096,
+                        hq=32, hkv=4, page=64)
+    wl = W.make_workload(spec, device="cuda")
+    _, gcfg = cfgs(spec, wl)
+    assert Q.gqa_splits(gcfg, spec.rows, spec.packed_width) == 2
+    st = OracleState(wl, with_kv=False)
+    rng = np.random.default_rng(43)
+    packed_np = random_packed(rng, st.cfg, st.logical_positions,
+                              full_rows=set(range(0, spec.rows, 2)))
+    assert int(packed_np[:, -1].max()) > 2560
+    out = torch.full_like(wl["q"], 3.0)
+    ws = torch.empty(1 << 26, dtype=torch.uint8, device="cuda")  # split partials and tickets
+    Q.sparse_gqa(gcfg, wl["q"], wl["kv"], wl["block_table"], torch.from_numpy(packed_np).cuda(),
+                 wl["token_to_req"], wl["gate"], out, ws)
+    torch.cuda.synchronize()
+    assert Q.check_errors() == 0
+    got = f64(out)
+    for row in (0, 1, 2, 3, rows_per, spec.rows // 2 + 1, spec.rows - 2, spec.rows - 1):
+        n = int(packed_np[row, -1])
+        req = int(st.token_to_req[row])
+        want = oracle_gqa_row(st.q[row], wl["kv"], st.block_table[req], packed_np[row, :n],
+                              spec.page, st.gate[row])
+        ok, err = close_bf16(got[row], want)
+        assert ok, f"row {row} (n={n}): max err {err:.3g}"
+
+
 # ----------------------------------------------------------------- full chain
 def _full_chain(spec, wl, st, step, rows=None, packed_ref=None, skip=False):
     """Compare a finished GPU step with the oracle's own chain on `rows`."""
